@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark: absorbed MLA decode tokens/s on one B300, with the latent-cache
+stream's roofline fraction.
+
+A step is one decode step of one MLA layer for every sequence of the workload:
+cache append of the new token(s) -> absorbed decode (fold, split-K attention,
+merge) -> W_UV up-projection, all through the C ABI.  Default workload: the
+DeepSeek-V3-shaped decode (hidden 7168, 128 heads, d_h 128, d_c 512, d_r 64,
+batch 64, 4096 cached rows + 1 new token per sequence, bf16, seed 2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (weak scaling; the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode tokens/s (1 B300) and latent-cache HBM GB/s as % of roofline"
+UNIT = "tokens/s"
+DOMINANT_KERNEL_SOURCES = ["head_latent_attention_25_b300/csrc/mla_decode_simt.cu"]
+DOMINANT_KERNEL_NAME = "split_simt_kernel"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="v3_b64_l4096")
+    p.add_argument("--num-splits", type=int, default=0)
+    p.add_argument("--sweep", action="store_true", help="one line per sweep point (not the contract line)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, kept with their times."""
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", device_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summary(rows, t0, t1):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sel = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.05]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel)}
+
+
+# ---------------------------------------------------------------- evidence from ncu
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in DOMINANT_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{DOMINANT_KERNEL_NAME}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, budget_s: float):
+    """Explicit (K/V materialising) oracle over whole sequences until the budget is spent."""
+    import mla_inputs
+    from oracle import oracle_sequence
+    weights, h, queries = mla_inputs.make_all(wl)
+    lens = mla_inputs.context_lengths(wl)
+    t0 = time.perf_counter()
+    n = 0
+    while n < wl.batch:
+        oracle_sequence(wl, weights, h, queries, n, lens[n])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} of {wl.batch} sequences of {wl.name}, all {wl.n_heads} heads, whole step "
+                      f"(append + explicit decode + W_UV), fp64, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- workload facts
+def workload_facts(wl, lens):
+    rows = sum(n + wl.n_new for n in lens)
+    row_bytes = (wl.d_c + wl.d_r) * (2 if wl.dtype == "bf16" else 4)
+    flops_per_row = 2 * wl.n_heads * ((wl.d_c + wl.d_r) + wl.d_c)
+    return rows, rows * row_bytes, rows * flops_per_row
+
+
+def config_of(wl, lens, extra=None):
+    c = {"workload": wl.name, "batch": wl.batch, "n_heads": wl.n_heads, "d_h": wl.d_h, "d_c": wl.d_c,
+         "d_r": wl.d_r, "hidden": wl.hidden, "context_rows": (lens[0] if wl.ragged is None else
+                                                               [int(min(lens)), int(max(lens))]),
+         "new_tokens_per_seq": wl.n_new, "seed": wl.seed,
+         "l2": "inputs larger than L2 (latent cache plus weights exceed 126 MB); no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, wl, rank, world):
+    import torch
+    import torch.distributed as dist
+    import mla_inputs
+    from head_latent_attention_25_b300 import runner, mla_launch_count, mla_profile_events
+
+    dev = torch.cuda.current_device()
+    lens = mla_inputs.context_lengths(wl)
+    st = runner.from_workload(wl, ctx_lens=lens, num_splits=args.num_splits)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(dev)
+    sampler = ClockSampler(uuid) if rank == 0 else None
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) == 0, "device status set during warm-up"
+
+    K = args.steps
+    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev_split:               # torch creates the CUDA event on its first record
+        a.record(stream)
+        b.record(stream)
+    t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    n0 = mla_launch_count()
+    wall0 = time.time()
+    t_beg.record(stream)
+    for i in range(K):
+        mla_profile_events(*ev_split[i])
+        st.step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier()
+    mla_profile_events(None, None)
+    launches = mla_launch_count() - n0
+    ms = max_over_ranks(t_beg.elapsed_time(t_end))
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_split)
+    clocks = ClockSampler.summary(sampler.stop(), wall0, wall1) if sampler else None
+    assert int(st.dev_status.item()) == 0
+
+    # end to end: inputs from pinned host memory each step, result read back each step
+    h_host = st.h.cpu().pin_memory()
+    qc_host, qr_host = st.q_c.cpu().pin_memory(), st.q_r.cpu().pin_memory()
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    h2d = h_host.numel() * h_host.element_size()
+    if not wl.query_from_h:
+        h2d += qc_host.numel() * qc_host.element_size() + qr_host.numel() * qr_host.element_size()
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        st.h.copy_(h_host, non_blocking=True)
+        if wl.query_from_h:
+            st.x_q.copy_(st.h[:, -1, :])
+        else:
+            st.q_c.copy_(qc_host, non_blocking=True)
+            st.q_r.copy_(qr_host, non_blocking=True)
+        st.step()
+        out_host.copy_(st.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e_beg, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e_beg.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e_beg.elapsed_time(e_end))
+
+    if rank != 0:
+        return None
+    rows, cache_bytes, flops = workload_facts(wl, lens)
+    hbm, tf_burst, tf_sus, src = peaks()
+    split_s = split_ms / 1e3
+    gbs = cache_bytes / split_s / 1e9
+    tfs = flops / split_s / 1e12
+    tokens = wl.batch * world * K
+    value = tokens / (ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded N(0,0.02) weights and cache)",
+        "config": config_of(wl, lens, {"parallelism": "replicas" if world > 1 else "single_gpu",
+                                       "num_splits": args.num_splits or "auto"}),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": ncu_traffic(wl.name), "kernel": DOMINANT_KERNEL_NAME,
+                     "peak_source": f"{src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": cache_bytes, "kernel_ms": split_ms},
+        "roofline_tensor": {"achieved": tfs, "unit": "TFLOP/s", "peak_burst": tf_burst,
+                            "peak_sustained": tf_sus, "frac_burst": tfs / tf_burst,
+                            "frac_sustained": tfs / tf_sus, "algorithmic_flops_per_launch": flops},
+        "cache_gbs_step": cache_bytes / (ms / K / 1e3) / 1e9,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, wl):
+    """The oracle as it stands, timed on the host cores: each step decodes one sequence
+    over a subset of heads sized so the whole run stays within a few minutes."""
+    import mla_inputs
+    from oracle import oracle_sequence
+    weights, h, queries = mla_inputs.make_all(wl)
+    lens = mla_inputs.context_lengths(wl)
+    t = time.perf_counter()
+    oracle_sequence(wl, weights, h, queries, 0, lens[0], heads=list(range(min(4, wl.n_heads))))
+    per_head = (time.perf_counter() - t) / min(4, wl.n_heads)
+    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+    n_heads = max(1, min(wl.n_heads, int(budget_per_step / max(per_head, 1e-9))))
+    heads = list(range(n_heads))
+    for i in range(args.warmup):
+        b = i % wl.batch
+        oracle_sequence(wl, weights, h, queries, b, lens[b], heads=heads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        b = i % wl.batch
+        oracle_sequence(wl, weights, h, queries, b, lens[b], heads=heads)
+    dt = time.perf_counter() - t0
+    value = args.steps * (n_heads / wl.n_heads) / dt
+    sample = (f"each step: one sequence of {wl.name} ({n_heads} of {wl.n_heads} heads, "
+              f"counted as {n_heads}/{wl.n_heads} token), append + explicit decode + W_UV, fp64")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,0.02) weights and cache)", "config": config_of(wl, lens),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    import mla_inputs
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    wl = mla_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    if args.sweep:
+        for w in mla_inputs.sweep_workloads():
+            line = run_ours(args, w, rank, world)
+            if line:
+                print(json.dumps(line), flush=True)
+            torch.cuda.empty_cache()
+    else:
+        line = run_ours(args, wl, rank, world)
+        if line:
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+"""ctypes binding of ``libmla.so`` (argument marshalling only).
+
+Every function here has the name and argument order of the C entry point in
+``include/mla.h``.  Tensor arguments may be torch tensors (their ``data_ptr()`` is
+passed) or integer addresses.  Nothing is computed here: every step runs in the
+CUDA library, and loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla.so")
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA = range(5)
+MLA_F32, MLA_BF16 = 0, 1
+MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
+            "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",
+            "mla_profile_events")
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int32), ("d_h", ctypes.c_int32), ("d_c", ctypes.c_int32),
+                ("d_r", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("rope_base", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load():
+    """The loaded library; raises if ``libmla.so`` is missing (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run `python -m head_latent_attention_25_b300.build`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(MlaDims)
+    lib.mla_cache_append.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P, P, P]
+    lib.mla_cache_append.restype = I32
+    lib.mla_project_query.argtypes = [D, I32, I32, I32, P, P, P, P, P, P]
+    lib.mla_project_query.restype = I32
+    lib.mla_decode_workspace_size.argtypes = [D, I32, I32, I32, I32]
+    lib.mla_decode_workspace_size.restype = SZ
+    lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, P, P, I32, I32, P, SZ, P, P, P, P]
+    lib.mla_decode_absorbed.restype = I32
+    lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P]
+    lib.mla_project_out.restype = I32
+    lib.mla_status_string.argtypes = [I32]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_launch_count.argtypes = []
+    lib.mla_launch_count.restype = ctypes.c_uint64
+    lib.mla_profile_events.argtypes = [P, P]
+    lib.mla_profile_events.restype = I32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().mla_status_string(int(status)).decode()
+
+
+def _p(x):
+    """Device address of a tensor (or None / int passthrough)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, status):
+    if status != MLA_OK:
+        raise MlaError(fn, status)
+
+
+def make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base=10000.0, softmax_scale=0.0) -> MlaDims:
+    return MlaDims(n_heads, d_h, d_c, d_r, hidden, rope_base, softmax_scale)
+
+
+def mla_cache_append(dims, dtype, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cache,
+                     dev_status, stream=None):
+    _check("mla_cache_append", load().mla_cache_append(
+        ctypes.byref(dims), dtype, batch, n_new, _p(h), _p(w_dkv), _p(w_kr), _p(row_off), _p(cap),
+        _p(pos0), _p(cache), _p(dev_status), _stream(stream)))
+
+
+def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, stream=None):
+    _check("mla_project_query", load().mla_project_query(
+        ctypes.byref(dims), dtype, batch, d_in, _p(x), _p(w_uq), _p(w_qr), _p(q_c), _p(q_r),
+        _stream(stream)))
+
+
+def mla_decode_workspace_size(dims, dtype, batch, max_seq_len, num_splits=0) -> int:
+    return int(load().mla_decode_workspace_size(ctypes.byref(dims), dtype, batch, max_seq_len,
+                                                num_splits))
+
+
+def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, row_off, seq_len, max_seq_len,
+                        num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream=None):
+    _check("mla_decode_absorbed", load().mla_decode_absorbed(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), _p(row_off),
+        _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes, _p(o_lat), _p(lse),
+        _p(dev_status), _stream(stream)))
+
+
+def mla_project_out(dims, dtype, batch, o_lat, w_uv, out, stream=None):
+    _check("mla_project_out", load().mla_project_out(
+        ctypes.byref(dims), dtype, batch, _p(o_lat), _p(w_uv), _p(out), _stream(stream)))
+
+
+def mla_launch_count() -> int:
+    return int(load().mla_launch_count())
+
+
+def mla_profile_events(start, stop):
+    """``start``/``stop``: torch.cuda.Event (timing enabled), raw handles, or None."""
+    def h(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    _check("mla_profile_events", load().mla_profile_events(h(start), h(stop)))

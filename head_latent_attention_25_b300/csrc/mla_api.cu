@@ -1,0 +1,204 @@
+// C-ABI entry points: argument checks, workspace planning and kernel dispatch.
+#include <math.h>
+
+#include <atomic>
+
+#include "mla_common.cuh"
+#include "mla_internal.h"
+
+using namespace mla;
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+thread_local cudaEvent_t t_ev_start = nullptr;
+thread_local cudaEvent_t t_ev_stop = nullptr;
+
+}  // namespace
+
+namespace mla {
+
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+void profile_before_split(cudaStream_t s) {
+    if (t_ev_start) cudaEventRecord(t_ev_start, s);
+}
+
+void profile_after_split(cudaStream_t s) {
+    if (t_ev_stop) cudaEventRecord(t_ev_stop, s);
+}
+
+}  // namespace mla
+
+namespace {
+
+bool dims_ok(const mla_dims* d) {
+    if (!d) return false;
+    if (d->n_heads < 1 || d->d_h < 1 || d->d_c < 2 || d->d_r < 2 || d->hidden < 1) return false;
+    if ((d->d_c & 1) || (d->d_r & 1)) return false;
+    if (!(d->rope_base > 0.f) || !isfinite(d->rope_base)) return false;
+    if (!(d->softmax_scale >= 0.f) || !isfinite(d->softmax_scale)) return false;
+    if ((int64_t)d->n_heads * d->d_h > (1 << 24) || d->d_c > 65536 || d->d_r > 65536) return false;
+    return true;
+}
+
+bool dtype_ok(mla_dtype t) { return t == MLA_F32 || t == MLA_BF16; }
+size_t elt(mla_dtype t) { return t == MLA_BF16 ? 2 : 4; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+float scale_of(const mla_dims* d) {
+    return d->softmax_scale > 0.f ? d->softmax_scale : 1.f / sqrtf((float)(d->d_h + d->d_r));
+}
+
+// Largest latent width the SIMT decode keeps in registers (16 columns per lane).
+constexpr int kSimtMaxDc = 512;
+
+bool simt_supported(const mla_dims* d) {
+    return d->d_c <= kSimtMaxDc && (d->d_c + d->d_r) <= 1024;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+struct DecodePlan {
+    int workers;
+    DecodeWorkspace ws;
+};
+
+bool plan_decode(const mla_dims* d, mla_dtype t, int batch, int max_seq_len, int num_splits,
+                 DecodePlan* p) {
+    if (!dims_ok(d) || !dtype_ok(t) || batch < 1 || max_seq_len < 0 || num_splits < 0) return false;
+    if (!simt_supported(d)) return false;
+    int w = num_splits;
+    if (w == 0) {
+        const int sms = sm_count();
+        if (sms <= 0) return false;
+        w = simt_workers(batch, d->n_heads, (int64_t)batch * (max_seq_len > 0 ? max_seq_len : 1), sms);
+    }
+    if (w > (1 << 20)) return false;
+    p->workers = w;
+    DecodeWorkspace& ws = p->ws;
+    const size_t A = 256;
+    const int dq = d->d_c + d->d_r;
+    size_t off = 0;
+    ws.q_off = off;     ws.q_bytes = (size_t)batch * d->n_heads * dq * sizeof(float);
+    off = align_up(off + ws.q_bytes, A);
+    ws.cum_off = off;   ws.cum_bytes = (size_t)(batch + 1) * sizeof(int64_t);
+    off = align_up(off + ws.cum_bytes, A);
+    ws.sched_off = off; ws.sched_bytes = sizeof(Schedule);
+    off = align_up(off + ws.sched_bytes, A);
+    ws.po_off = off;    ws.po_bytes = (size_t)2 * w * d->n_heads * d->d_c * sizeof(float);
+    off = align_up(off + ws.po_bytes, A);
+    ws.pl_off = off;    ws.pl_bytes = (size_t)2 * w * d->n_heads * sizeof(float);
+    off = align_up(off + ws.pl_bytes, A);
+    ws.total = off;
+    return true;
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported dims/dtype";
+        case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MLA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+uint64_t mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mla_status mla_profile_events(void* start, void* stop) {
+    if ((start == nullptr) != (stop == nullptr)) return MLA_ERR_INVALID_ARG;
+    t_ev_start = (cudaEvent_t)start;
+    t_ev_stop = (cudaEvent_t)stop;
+    return MLA_OK;
+}
+
+mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
+                            const void* h, const void* w_dkv, const void* w_kr,
+                            const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
+                            void* cache, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+    if (!h || !w_dkv || !w_kr || !row_off || !cap || !pos0 || !cache || !dev_status)
+        return MLA_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
+    if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_append(*dims, dtype == MLA_BF16, batch, n_new, h, w_dkv, w_kr,
+                                     row_off, cap, pos0, cache, dev_status, (cudaStream_t)stream));
+}
+
+mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
+                             const void* x, const void* w_uq, const void* w_qr, void* q_c,
+                             void* q_r, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || d_in < 1) return MLA_ERR_INVALID_ARG;
+    if (!x || !w_uq || !w_qr || !q_c || !q_r) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_project_query(*dims, dtype == MLA_BF16, batch, d_in, x, w_uq, w_qr,
+                                            q_c, q_r, (cudaStream_t)stream));
+}
+
+size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                 int32_t max_seq_len, int32_t num_splits) {
+    DecodePlan p;
+    if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, &p)) return 0;
+    return p.ws.total;
+}
+
+mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                               const void* q_c, const void* q_r, const void* w_uk,
+                               const void* cache, const int64_t* row_off, const int32_t* seq_len,
+                               int32_t max_seq_len, int32_t num_splits, void* workspace,
+                               size_t workspace_bytes, void* o_lat, float* lse,
+                               int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || max_seq_len < 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+    if (!q_c || !q_r || !w_uk || !cache || !row_off || !seq_len || !o_lat || !dev_status)
+        return MLA_ERR_INVALID_ARG;
+    const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
+    if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
+    if (!simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
+    DecodePlan p;
+    if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, &p)) return MLA_ERR_CUDA;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < p.ws.total)
+        return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    float* qp = (float*)(ws + p.ws.q_off);
+    int64_t* cum = (int64_t*)(ws + p.ws.cum_off);
+    void* sched = ws + p.ws.sched_off;
+    float* part_o = (float*)(ws + p.ws.po_off);
+    float* part_l = (float*)(ws + p.ws.pl_off);
+    const bool bf16 = dtype == MLA_BF16;
+    const float alpha = scale_of(dims) * kLog2e;
+    cudaError_t e = launch_fold(*dims, bf16, false, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
+    if (e == cudaSuccess) e = launch_schedule(seq_len, batch, p.workers, cum, sched, s);
+    if (e == cudaSuccess)
+        e = launch_split_simt(*dims, bf16, batch, p.workers, qp, cache, row_off, seq_len, cum,
+                              sched, o_lat, lse, part_o, part_l, s);
+    if (e == cudaSuccess)
+        e = launch_merge(*dims, bf16, batch, seq_len, cum, sched, part_o, part_l, o_lat, lse,
+                         dev_status, s);
+    return cuda_status(e);
+}
+
+mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o_lat,
+                           const void* w_uv, void* out, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || !o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_project_out(*dims, dtype == MLA_BF16, batch, o_lat, w_uv, out,
+                                          (cudaStream_t)stream));
+}
+
+}  // extern "C"

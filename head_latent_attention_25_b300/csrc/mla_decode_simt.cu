@@ -1,0 +1,281 @@
+// Split-K decode over the latent cache, CUDA-core (SIMT) variant, plus the pieces
+// every decode variant shares: the work schedule and the merge of cut sequences.
+//
+// Scores are taken against the folded query Q' = alpha * [W_UK^T q_C ; RoPE(q_R)]
+// with alpha = softmax_scale * log2(e), so exp2 of a score difference is the
+// softmax ratio.  Each (worker, head) keeps a running maximum m, running sum l and
+// an unnormalised latent accumulator, rescaled whenever m grows (online softmax).
+#include <math.h>
+
+#include "mla_common.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+// ------------------------------------------------------------------ schedule
+__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len, int batch,
+                                                        int workers, int64_t* cum,
+                                                        Schedule* sched) {
+    __shared__ long long warp_tot[32];
+    __shared__ long long carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < batch; base += 1024) {
+        const int i = base + tid;
+        long long x = (i < batch) ? (long long)max(seq_len[i], 0) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                long long y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const long long incl = carry + (warp ? warp_tot[warp - 1] : 0) + x;
+        if (i < batch) cum[i + 1] = incl;
+        __syncthreads();
+        if (tid == 1023) carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        cum[0] = 0;
+        Schedule s;
+        s.total = carry;
+        s.workers = workers;
+        s.batch = batch;
+        s.per = carry > 0 ? (carry + workers - 1) / workers : 1;
+        *sched = s;
+    }
+}
+
+// ------------------------------------------------------------------ SIMT split
+constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
+
+struct SplitArgs {
+    const float* qp; const void* cache; const int64_t* row_off; const int64_t* cum;
+    const Schedule* sched; void* o_lat; float* lse; float* part_o; float* part_l;
+    int n_h, d_c, d_r, batch;
+};
+
+template <typename Tc>
+__global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
+    extern __shared__ float smem[];
+    const int dq = a.d_c + a.d_r;
+    const int ts = dq + 1;                      // odd stride: lane j reading row j is conflict-free
+    float* tile = smem;                         // [kTileRows][ts]
+    float* qs = smem + kTileRows * ts;          // [kWarps][dq]
+    const Schedule S = *a.sched;
+    const int g = blockIdx.x;
+    const int64_t begin = (int64_t)g * S.per;
+    const int64_t end = min(begin + S.per, S.total);
+    if (begin >= end) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y * kWarps + warp;
+    const bool active = h < a.n_h;
+    const Tc* cache = (const Tc*)a.cache;
+
+    int lo = 0, hi = a.batch - 1;               // last sequence whose rows start at or before begin
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (a.cum[mid] <= begin) lo = mid; else hi = mid - 1;
+    }
+    int b = lo;
+    int64_t cur = begin;
+    bool first = true;
+    while (cur < end) {
+        while (a.cum[b + 1] <= cur) ++b;
+        const int64_t seq0 = a.cum[b];
+        const int64_t len = a.cum[b + 1] - seq0;
+        const int64_t r_lo = cur - seq0;
+        const int64_t r_hi = min(len, end - seq0);
+        __syncthreads();                        // previous segment done with qs / tile
+        if (active)
+            for (int k = lane; k < dq; k += 32)
+                qs[warp * dq + k] = a.qp[((int64_t)b * a.n_h + h) * dq + k];
+        float m = -INFINITY, l = 0.f;
+        float acc[kMaxColsPerLane];
+#pragma unroll
+        for (int t = 0; t < kMaxColsPerLane; ++t) acc[t] = 0.f;
+        const Tc* rows = cache + a.row_off[b] * dq;
+        for (int64_t r0 = r_lo; r0 < r_hi; r0 += kTileRows) {
+            const int nr = (int)min((int64_t)kTileRows, r_hi - r0);
+            __syncthreads();
+            for (int e = tid; e < nr * dq; e += kWarps * 32) {
+                const int j = e / dq, k = e - j * dq;
+                tile[j * ts + k] = ld(rows + (r0 + j) * dq + k);
+            }
+            __syncthreads();
+            if (!active) continue;
+            float s = -INFINITY;
+            if (lane < nr) {
+                const float* row = tile + lane * ts;
+                const float* q = qs + warp * dq;
+                float acc_s = 0.f;
+                for (int k = 0; k < dq; ++k) acc_s = fmaf(q[k], row[k], acc_s);
+                s = acc_s;
+            }
+            const float mn = fmaxf(m, warp_max(s));
+            const float alpha = exp2f(m - mn);
+            const float p = (lane < nr) ? exp2f(s - mn) : 0.f;
+            l = l * alpha + warp_sum(p);
+#pragma unroll
+            for (int t = 0; t < kMaxColsPerLane; ++t) acc[t] *= alpha;
+            for (int j = 0; j < nr; ++j) {
+                const float pj = __shfl_sync(0xffffffffu, p, j);
+                const float* row = tile + j * ts;
+#pragma unroll
+                for (int t = 0; t < kMaxColsPerLane; ++t) {
+                    const int c = lane + 32 * t;
+                    if (c < a.d_c) acc[t] = fmaf(pj, row[c], acc[t]);
+                }
+            }
+            m = mn;
+        }
+        if (active) {
+            const float inv = 1.f / l;
+            const float lse2 = m + log2f(l);
+            if (r_lo == 0 && r_hi == len) {     // whole sequence here: final output
+                const int64_t o = ((int64_t)b * a.n_h + h) * a.d_c;
+                if (a.lse && lane == 0) a.lse[(int64_t)b * a.n_h + h] = lse2 * kLn2;
+#pragma unroll
+                for (int t = 0; t < kMaxColsPerLane; ++t) {
+                    const int c = lane + 32 * t;
+                    if (c < a.d_c) {
+                        if (sizeof(Tc) == 2) st((__nv_bfloat16*)a.o_lat + o + c, acc[t] * inv);
+                        else st((float*)a.o_lat + o + c, acc[t] * inv);
+                    }
+                }
+            } else {
+                const int64_t slot = 2 * (int64_t)g + (first ? 0 : 1);
+                const int64_t o = (slot * a.n_h + h) * a.d_c;
+                if (lane == 0) a.part_l[slot * a.n_h + h] = lse2;
+#pragma unroll
+                for (int t = 0; t < kMaxColsPerLane; ++t) {
+                    const int c = lane + 32 * t;
+                    if (c < a.d_c) a.part_o[o + c] = acc[t] * inv;
+                }
+            }
+        }
+        cur = seq0 + r_hi;
+        first = false;
+    }
+}
+
+// ------------------------------------------------------------------ merge
+template <typename Tout>
+__global__ void __launch_bounds__(128) merge_kernel(const int32_t* seq_len, const int64_t* cum,
+                                                    const Schedule* sched, const float* part_o,
+                                                    const float* part_l, Tout* o_lat, float* lse,
+                                                    int32_t* dev_status, int n_h, int d_c) {
+    const int bh = blockIdx.x;
+    const int b = bh / n_h, h = bh - b * n_h;
+    Tout* out = o_lat + (int64_t)bh * d_c;
+    if (seq_len[b] < 1) {
+        for (int c = threadIdx.x; c < d_c; c += blockDim.x) st(out + c, 0.f);
+        if (threadIdx.x == 0) {
+            if (lse) lse[bh] = -INFINITY;
+            if (h == 0) atomicOr(dev_status, MLA_DEV_BAD_LENGTH);
+        }
+        return;
+    }
+    const int64_t per = sched->per;
+    const int64_t first_w = cum[b] / per, last_w = (cum[b + 1] - 1) / per;
+    if (first_w == last_w) return;              // finished in place by its only worker
+    float mx = -INFINITY;
+    for (int64_t w = first_w; w <= last_w; ++w) {
+        const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
+        mx = fmaxf(mx, part_l[slot * n_h + h]);
+    }
+    float L = 0.f;
+    for (int64_t w = first_w; w <= last_w; ++w) {
+        const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
+        L += exp2f(part_l[slot * n_h + h] - mx);
+    }
+    const float inv = 1.f / L;
+    for (int c = threadIdx.x; c < d_c; c += blockDim.x) {
+        float v = 0.f;
+        for (int64_t w = first_w; w <= last_w; ++w) {
+            const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
+            v = fmaf(exp2f(part_l[slot * n_h + h] - mx), part_o[(slot * n_h + h) * d_c + c], v);
+        }
+        st(out + c, v * inv);
+    }
+    if (threadIdx.x == 0 && lse) lse[bh] = (mx + log2f(L)) * kLn2;
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const int32_t* seq_len, int batch, int workers, int64_t* cum,
+                            void* sched, cudaStream_t s) {
+    schedule_kernel<<<1, 1024, 0, s>>>(seq_len, batch, workers, cum, (Schedule*)sched);
+    note_launch();
+    return cudaGetLastError();
+}
+
+int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count) {
+    const int groups = (n_heads + kWarps - 1) / kWarps;
+    int64_t w = (2LL * sm_count + groups - 1) / groups;
+    const int64_t by_rows = (max_total_rows + kTileRows - 1) / kTileRows;
+    if (w > by_rows) w = by_rows;
+    if (w < 1) w = 1;
+    (void)batch;
+    return (int)w;
+}
+
+cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
+                              const void* cache, const int64_t* row_off, const int32_t* seq_len,
+                              const int64_t* cum, const void* sched, void* o_lat, float* lse,
+                              float* part_o, float* part_l, cudaStream_t s) {
+    (void)seq_len;
+    SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, o_lat, lse, part_o, part_l,
+                d.n_heads, d.d_c, d.d_r, batch};
+    const int dq = d.d_c + d.d_r;
+    const size_t smem = (size_t)(kTileRows * (dq + 1) + kWarps * dq) * sizeof(float);
+    dim3 grid(workers, (d.n_heads + kWarps - 1) / kWarps);
+    cudaError_t e;
+    if (bf16) {
+        e = cudaFuncSetAttribute(split_simt_kernel<__nv_bfloat16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        profile_before_split(s);
+        split_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, smem, s>>>(a);
+    } else {
+        e = cudaFuncSetAttribute(split_simt_kernel<float>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        profile_before_split(s);
+        split_simt_kernel<float><<<grid, kWarps * 32, smem, s>>>(a);
+    }
+    profile_after_split(s);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int32_t* seq_len,
+                         const int64_t* cum, const void* sched, const float* part_o,
+                         const float* part_l, void* o_lat, float* lse, int32_t* dev_status,
+                         cudaStream_t s) {
+    const int blocks = batch * d.n_heads;
+    if (bf16)
+        merge_kernel<<<blocks, 128, 0, s>>>(seq_len, cum, (const Schedule*)sched, part_o, part_l,
+                                            (__nv_bfloat16*)o_lat, lse, dev_status, d.n_heads, d.d_c);
+    else
+        merge_kernel<<<blocks, 128, 0, s>>>(seq_len, cum, (const Schedule*)sched, part_o, part_l,
+                                            (float*)o_lat, lse, dev_status, d.n_heads, d.d_c);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,53 @@
+// Launch helpers shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+struct DecodeWorkspace;
+
+cudaError_t launch_append(const mla_dims& d, bool bf16, int batch, int n_new, const void* h,
+                          const void* w_dkv, const void* w_kr, const int64_t* row_off,
+                          const int32_t* cap, const int32_t* pos0, void* cache, int32_t* dev_status,
+                          cudaStream_t s);
+
+cudaError_t launch_project_query(const mla_dims& d, bool bf16, int batch, int d_in, const void* x,
+                                 const void* w_uq, const void* w_qr, void* q_c, void* q_r,
+                                 cudaStream_t s);
+
+// Q'[b, i, :] = alpha * [W_UK^(i)T q_C[b,i] ; RoPE(q_R[b,i], seq_len[b]-1)]
+cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_c,
+                        const void* q_r, const void* w_uk, const int32_t* seq_len, float alpha,
+                        void* qp, cudaStream_t s);
+
+cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const void* o_lat,
+                               const void* w_uv, void* out, cudaStream_t s);
+
+// Work split of the flattened context: prefix sums + Schedule into the workspace.
+cudaError_t launch_schedule(const int32_t* seq_len, int batch, int workers, int64_t* cum,
+                            void* sched, cudaStream_t s);
+
+// fp32-Q' SIMT split kernel (any supported dims, fp32 or bf16 cache).
+cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
+                              const void* cache, const int64_t* row_off, const int32_t* seq_len,
+                              const int64_t* cum, const void* sched, void* o_lat, float* lse,
+                              float* part_o, float* part_l, cudaStream_t s);
+
+// Combines the partial results of sequences cut across workers; flags empty sequences.
+cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int32_t* seq_len,
+                         const int64_t* cum, const void* sched, const float* part_o,
+                         const float* part_l, void* o_lat, float* lse, int32_t* dev_status,
+                         cudaStream_t s);
+
+// Launch accounting and the optional per-thread timing hook around the split kernel.
+void note_launch(int n = 1);
+void profile_before_split(cudaStream_t s);
+void profile_after_split(cudaStream_t s);
+
+int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count);
+
+}  // namespace mla

@@ -1,0 +1,140 @@
+"""One decode step of one MLA layer over resident device buffers.
+
+``DecodeStep`` owns the device memory of a batch of sequences (latent cache,
+index arrays, workspace, outputs; torch allocates it) and enqueues the path
+through the C ABI: cache append -> [query projection] -> absorbed decode ->
+W_UV projection.  It computes nothing itself.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib as L
+
+
+class DecodeStep:
+    """Device buffers and C-ABI calls of one decode step for ``batch`` sequences.
+
+    ``ctx_lens[b]`` rows are already in the cache before the step; ``n_new``
+    tokens are appended at positions ctx_lens[b] .. ctx_lens[b]+n_new-1, and the
+    query (position ctx_lens[b]+n_new-1) attends over ctx_lens[b]+n_new rows.
+    """
+
+    def __init__(self, *, n_heads: int, d_h: int, d_c: int, d_r: int, hidden: int,
+                 dtype: str, ctx_lens: Sequence[int], n_new: int, rope_base: float = 10000.0,
+                 softmax_scale: float = 0.0, query_from_h: bool = False, d_q_in: Optional[int] = None,
+                 num_splits: int = 0, extra_rows: int = 0, device: str = "cuda"):
+        L.load()
+        self.dims = L.make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base, softmax_scale)
+        self.dt = L.MLA_BF16 if dtype == "bf16" else L.MLA_F32
+        self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.batch = B = len(ctx_lens)
+        self.n_new = n_new
+        self.ctx_lens = [int(x) for x in ctx_lens]
+        self.query_from_h = query_from_h
+        self.d_q_in = d_q_in if d_q_in is not None else hidden
+        self.row_elems = d_c + d_r
+        self.device = device
+        caps = [c + n_new + extra_rows for c in self.ctx_lens]
+        offs, o = [], 0
+        for c in caps:
+            offs.append(o)
+            o += c
+        self.total_rows = o
+        self.row_off = torch.tensor(offs, dtype=torch.int64, device=device)
+        self.cap = torch.tensor(caps, dtype=torch.int32, device=device)
+        self.pos0 = torch.tensor(self.ctx_lens, dtype=torch.int32, device=device)
+        self.seq_len = torch.tensor([c + n_new for c in self.ctx_lens], dtype=torch.int32, device=device)
+        self.max_seq_len = max(c + n_new for c in self.ctx_lens)
+        self.cache = torch.zeros(self.total_rows, self.row_elems, dtype=self.tdt, device=device)
+        self.h = torch.zeros(B, n_new, hidden, dtype=self.tdt, device=device)
+        self.q_c = torch.zeros(B, n_heads, d_h, dtype=self.tdt, device=device)
+        self.q_r = torch.zeros(B, n_heads, d_r, dtype=self.tdt, device=device)
+        self.x_q = torch.zeros(B, self.d_q_in, dtype=self.tdt, device=device) if query_from_h else None
+        self.o_lat = torch.zeros(B, n_heads, d_c, dtype=self.tdt, device=device)
+        self.lse = torch.zeros(B, n_heads, dtype=torch.float32, device=device)
+        self.out = torch.zeros(B, n_heads, d_h, dtype=self.tdt, device=device)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.num_splits = num_splits
+        self.ws_bytes = L.mla_decode_workspace_size(self.dims, self.dt, B, self.max_seq_len, num_splits)
+        if self.ws_bytes == 0:
+            raise L.MlaError("mla_decode_workspace_size", L.MLA_ERR_UNSUPPORTED)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.w = {}
+
+    # ------------------------------------------------------------------ inputs
+    def set_weights(self, weights: dict):
+        for k, v in weights.items():
+            self.w[k] = v.to(self.device, self.tdt).contiguous()
+
+    def set_prefill(self, b: int, rows: torch.Tensor):
+        n = rows.shape[0]
+        o = int(self.row_off[b].item())
+        self.cache[o:o + n].copy_(rows.to(self.tdt))
+
+    def set_tokens(self, h: torch.Tensor):
+        self.h.copy_(h)
+        if self.query_from_h:
+            self.x_q.copy_(h[:, -1, :])
+
+    def set_queries(self, q_c: torch.Tensor, q_r: torch.Tensor):
+        self.q_c.copy_(q_c)
+        self.q_r.copy_(q_r)
+
+    # ------------------------------------------------------------------ path
+    def append(self, stream=None):
+        L.mla_cache_append(self.dims, self.dt, self.batch, self.n_new, self.h, self.w["w_dkv"],
+                           self.w["w_kr"], self.row_off, self.cap, self.pos0, self.cache,
+                           self.dev_status, stream)
+
+    def project_query(self, stream=None):
+        L.mla_project_query(self.dims, self.dt, self.batch, self.d_q_in, self.x_q, self.w["w_uq"],
+                            self.w["w_qr"], self.q_c, self.q_r, stream)
+
+    def decode(self, stream=None, num_splits=None, o_lat=None, lse=None):
+        ns = self.num_splits if num_splits is None else num_splits
+        ws = self.workspace
+        if ns != self.num_splits:
+            nb = L.mla_decode_workspace_size(self.dims, self.dt, self.batch, self.max_seq_len, ns)
+            ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        L.mla_decode_absorbed(self.dims, self.dt, self.batch, self.q_c, self.q_r, self.w["w_uk"],
+                              self.cache, self.row_off, self.seq_len, self.max_seq_len, ns, ws,
+                              ws.numel(), self.o_lat if o_lat is None else o_lat,
+                              self.lse if lse is None else lse, self.dev_status, stream)
+
+    def project_out(self, stream=None):
+        L.mla_project_out(self.dims, self.dt, self.batch, self.o_lat, self.w["w_uv"], self.out, stream)
+
+    def step(self, stream=None):
+        """The whole path: append, [query projection], decode, up-projection."""
+        self.append(stream)
+        if self.query_from_h:
+            self.project_query(stream)
+        self.decode(stream)
+        self.project_out(stream)
+
+    def new_rows(self, b: int) -> torch.Tensor:
+        o = int(self.row_off[b].item()) + self.ctx_lens[b]
+        return self.cache[o:o + self.n_new]
+
+
+def from_workload(wl, ctx_lens=None, num_splits: int = 0, device: str = "cuda", load_inputs: bool = True):
+    """A ``DecodeStep`` for a synthetic workload, inputs uploaded from the seeded generators."""
+    import mla_inputs
+    if ctx_lens is None:
+        ctx_lens = mla_inputs.context_lengths(wl)
+    st = DecodeStep(n_heads=wl.n_heads, d_h=wl.d_h, d_c=wl.d_c, d_r=wl.d_r, hidden=wl.hidden,
+                    dtype=wl.dtype, ctx_lens=ctx_lens, n_new=wl.n_new, rope_base=wl.rope_base,
+                    query_from_h=wl.query_from_h, num_splits=num_splits, device=device)
+    if load_inputs:
+        weights, h, queries = mla_inputs.make_all(wl)
+        st.set_weights(weights)
+        st.set_tokens(h)
+        if queries is not None:
+            st.set_queries(*queries)
+        for b, n in enumerate(ctx_lens):
+            if n:
+                st.set_prefill(b, mla_inputs.make_prefill_rows(wl, b, n))
+    return st

@@ -1,0 +1,195 @@
+/*
+ * mla.h -- C ABI of the absorbed Multi-Head Latent Attention (MLA) decode library
+ * for NVIDIA B300 (sm_103a).
+ *
+ * The operations follow the column-vector equations of "Grouped-query and latent
+ * attention" (sections "Multi-head latent attention", "The absorption trick" and
+ * "Why a separate rotary key"):
+ *
+ *   c     = W_DKV h                      latent, d_c numbers, cached
+ *   k_R   = RoPE(W_KR h, pos)            rotary key, d_r numbers, cached, shared by heads
+ *   q'_i  = W_UK^(i)T q_C,i              query folded through the key up-projection
+ *   s_ij  = (q'_i . c_j + RoPE(q_R,i, p) . k_R,j) / sqrt(d_h + d_r)
+ *   o_lat_i = sum_j softmax_j(s_ij) c_j  latent weighted sum
+ *   o_i   = W_UV^(i) o_lat_i             value up-projection
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer (cudaMalloc'd or equivalent) except
+ *   `dims`, which points to host memory.  The caller owns all memory; the library
+ *   allocates nothing, frees nothing and never synchronises.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   Every call only enqueues work on that stream and returns.
+ * - Element type: `dtype` selects the storage type of weights, activations, the
+ *   latent cache and the outputs (fp32 or bf16).  Accumulation is always fp32.
+ *   `lse` is always fp32.
+ * - All arrays are dense row-major with the shapes given in brackets.  Weights use
+ *   the column convention y = W x, so W is [out, in]; the per-head blocks
+ *   W_UK^(i), W_UV^(i) (rows i*d_h .. (i+1)*d_h-1 of a (n_h*d_h) x d_c matrix)
+ *   are stored as [n_h, d_h, d_c].
+ * - Latent cache: one buffer of rows of (d_c + d_r) elements, each row laid out as
+ *   [c ; k_R] ("MLA storage", section "Storing a positional key separately").
+ *   Sequence b owns rows row_off[b] .. row_off[b] + cap[b] - 1; the token at
+ *   position t of sequence b is row row_off[b] + t.  The cache base pointer and
+ *   every row must be 16-byte aligned (row bytes a multiple of 16).
+ * - Errors the host can detect (null pointers, bad sizes, unsupported shapes, a
+ *   small workspace) are returned before anything is enqueued.  A failed launch
+ *   returns MLA_ERR_CUDA.  Conditions only the device can see are OR-ed into
+ *   *dev_status (MLA_DEV_* bits) and the affected outputs are left as documented;
+ *   read it after synchronising.  No kernel traps, asserts or waits without bound.
+ * - Rotary embedding pairs dimensions (2k, 2k+1) and turns them by pos*theta_k,
+ *   theta_k = rope_base^(-2k/d_r).  The query of a sequence holding n rows sits at
+ *   position n-1.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, misaligned buffer */
+    MLA_ERR_UNSUPPORTED = 2,  /* no kernel for this dims/dtype combination */
+    MLA_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than required */
+    MLA_ERR_CUDA = 4          /* a CUDA runtime call or a kernel launch failed */
+} mla_status;
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Bits OR-ed into *dev_status by kernels. */
+#define MLA_DEV_BAD_LENGTH   0x1  /* decode: seq_len[b] < 1; that sequence's outputs are zero, lse -inf */
+#define MLA_DEV_BAD_POSITION 0x2  /* append: pos0[b] < 0 or pos0[b] + n_new > cap[b]; rows of b not written */
+#define MLA_DEV_TIMEOUT      0x4  /* a bounded wait inside a kernel gave up; outputs undefined */
+
+typedef struct {
+    int32_t n_heads;      /* n_h: attention heads */
+    int32_t d_h;          /* per-head content key / value width */
+    int32_t d_c;          /* latent width (cached) */
+    int32_t d_r;          /* decoupled rotary key width (cached once per token), even */
+    int32_t hidden;       /* width of the token input h */
+    float rope_base;      /* rotary base, > 0 */
+    float softmax_scale;  /* 0 selects 1/sqrt(d_h + d_r) */
+} mla_dims;
+
+/*
+ * mla_cache_append -- write the latent rows of new tokens into the cache.
+ * Defines c = W_DKV h and k_R = RoPE(W_KR h, pos) ("Grouped-query and latent
+ * attention", sections "Multi-head latent attention" and "Why a separate rotary
+ * key"; "MLA storage", section "Storing a positional key separately").
+ *
+ *   h        [batch, n_new, hidden]   inputs of the new tokens
+ *   w_dkv    [d_c, hidden]            down-projection
+ *   w_kr     [d_r, hidden]            rotary key projection
+ *   row_off  [batch] int64            first cache row of each sequence
+ *   cap      [batch] int32            rows reserved for each sequence
+ *   pos0     [batch] int32            position of the first new token of each sequence
+ *   cache    rows of d_c + d_r        token t of sequence b goes to row
+ *                                     row_off[b] + pos0[b] + t, rotated at position pos0[b] + t
+ *   dev_status int32 (device)         MLA_DEV_BAD_POSITION is OR-ed in for a sequence whose
+ *                                     new rows would leave [0, cap[b]); its rows are skipped
+ * Row values are rounded once from the fp32 accumulator to `dtype`.
+ */
+MLA_API mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
+                            const void* h, const void* w_dkv, const void* w_kr,
+                            const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
+                            void* cache, int32_t* dev_status, void* stream);
+
+/*
+ * mla_project_query -- per-head query parts from a query input x (the query latent
+ * c_q, or h itself when the model has no query down-projection): q_C = W_UQ x and
+ * q_R = W_QR x, the latter NOT yet rotated (decode rotates it at the query's
+ * position).  ("Grouped-query and latent attention", sections "Multi-head latent
+ * attention" and "Why a separate rotary key".)
+ *
+ *   x     [batch, d_in]
+ *   w_uq  [n_h*d_h, d_in]       w_qr [n_h*d_r, d_in]
+ *   q_c   [batch, n_h, d_h]     q_r  [batch, n_h, d_r]
+ */
+MLA_API mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
+                             const void* x, const void* w_uq, const void* w_qr,
+                             void* q_c, void* q_r, void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode_absorbed needs
+ * for these arguments (the same batch, max_seq_len and num_splits must be passed to
+ * the decode call).  Returns 0 for arguments the decode would reject.
+ */
+MLA_API size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                 int32_t max_seq_len, int32_t num_splits);
+
+/*
+ * mla_decode_absorbed -- one decode query per sequence over that sequence's cached
+ * rows, with the key-side and value-side absorption ("Grouped-query and latent
+ * attention", section "The absorption trick"; scale from section "Why a separate
+ * rotary key").  Full per-head keys and values are never formed.
+ *
+ *   q_c      [batch, n_h, d_h]     content query
+ *   q_r      [batch, n_h, d_r]     rotary query, not yet rotated
+ *   w_uk     [n_h, d_h, d_c]       key up-projection
+ *   cache, row_off                 as for mla_cache_append
+ *   seq_len  [batch] int32         rows of each sequence (new token included); the query
+ *                                  sits at position seq_len[b]-1 and attends over rows
+ *                                  0 .. seq_len[b]-1
+ *   max_seq_len  host int           upper bound used only to size the split grid
+ *   num_splits   host int           number of context pieces the work is cut into
+ *                                  (0 = choose from the GPU's SM count); results do not
+ *                                  depend on it beyond fp32 rounding order
+ *   workspace    device buffer of at least mla_decode_workspace_size(...) bytes, 256-byte
+ *                aligned; contents on entry are ignored
+ *   o_lat    [batch, n_h, d_c]     out: sum_j a_ij c_j, in `dtype`
+ *   lse      [batch, n_h] fp32     out (may be NULL): natural log of sum_j exp(s_ij)
+ *   dev_status                     MLA_DEV_BAD_LENGTH for seq_len[b] < 1 (outputs of b
+ *                                  zero, lse -inf); MLA_DEV_TIMEOUT if a bounded wait
+ *                                  expired
+ */
+MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                               const void* q_c, const void* q_r, const void* w_uk,
+                               const void* cache, const int64_t* row_off, const int32_t* seq_len,
+                               int32_t max_seq_len, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes,
+                               void* o_lat, float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * mla_project_out -- o_i = W_UV^(i) o_lat_i for every head ("Grouped-query and
+ * latent attention", section "The absorption trick", value side).
+ *
+ *   o_lat [batch, n_h, d_c]    w_uv [n_h, d_h, d_c]    out [batch, n_h, d_h]
+ */
+MLA_API mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                           const void* o_lat, const void* w_uv, void* out, void* stream);
+
+/* Static description of a status code (never NULL). */
+MLA_API const char* mla_status_string(mla_status status);
+
+/*
+ * mla_launch_count -- number of kernels this library has enqueued in this process
+ * (all host threads, all devices), for accounting of what ran on the GPU.
+ */
+MLA_API uint64_t mla_launch_count(void);
+
+/*
+ * mla_profile_events -- optional timing hook.  While set, every mla_decode_absorbed
+ * call made from the CALLING HOST THREAD records `start` on its stream just before
+ * the attention (split) kernel and `stop` just after it, so the caller can read that
+ * kernel's own duration with cudaEventElapsedTime.  Both are cudaEvent_t handles
+ * passed as void*, created by the caller; (NULL, NULL) turns the hook off.  Returns
+ * MLA_ERR_INVALID_ARG when exactly one of them is NULL.
+ */
+MLA_API mla_status mla_profile_events(void* start, void* stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

@@ -52,7 +52,8 @@ class Workload:
     seed: int
     weight_std: Optional[float]     # None -> 1/sqrt(fan_in)
     cache_std: float = 0.02
-    act_std: float = 1.0            # std of h, q_C, q_R
+    act_std: float = 1.0            # std of h (and of q_C, q_R unless query_std is set)
+    query_std: Optional[float] = None
     query_from_h: bool = False      # q_C = W_UQ h, q_R = W_QR h (no query down-projection given)
     ragged: Optional[tuple] = None  # (low, high) inclusive bounds for ragged context lengths
     d_q: Optional[int] = None       # query latent width of the full model (not used by this path)
@@ -142,8 +143,9 @@ def _draw_all(wl: Workload):
     h = _normal(g, (wl.batch, wl.n_new, wl.hidden), wl.act_std, dt)
     q = None
     if not wl.query_from_h:
-        q_c = _normal(g, (wl.batch, wl.n_heads, wl.d_h), wl.act_std, dt)
-        q_r = _normal(g, (wl.batch, wl.n_heads, wl.d_r), wl.act_std, dt)
+        q_std = wl.act_std if wl.query_std is None else wl.query_std
+        q_c = _normal(g, (wl.batch, wl.n_heads, wl.d_h), q_std, dt)
+        q_r = _normal(g, (wl.batch, wl.n_heads, wl.d_r), q_std, dt)
         q = (q_c, q_r)
     return w, h, q
 

@@ -173,21 +173,22 @@ def decode_explicit(q_c, q_r, w_uk, w_uv, rows, base: float, scale=None) -> dict
         scale = softmax_scale(d_h, d_r)
     n = rows.shape[0]
     p = n - 1                                        # the new token's own position
-    keys = full_keys(rows, w_uk, d_c)                # [n, n_h, d_h + d_r]
-    _, values = expand_heads(rows[:, :d_c], w_uk, w_uv)   # [n, n_h, d_h]
+    w_uk, w_uv = f64(w_uk), f64(w_uv)
     q_rot = rope(q_r, p, base)
     o = np.zeros((n_h, d_h))
     o_lat = np.zeros((n_h, d_c))
     lse = np.zeros(n_h)
     a_all = np.zeros((n_h, n))
-    for i in range(n_h):
+    for i in range(n_h):                             # one head's K and V at a time (memory)
+        keys = full_keys(rows, w_uk[i:i + 1], d_c)[:, 0, :]                   # [n, d_h + d_r]
+        values = expand_heads(rows[:, :d_c], w_uk[i:i + 1], w_uv[i:i + 1])[1][:, 0, :]  # [n, d_h]
         q = np.concatenate([q_c[i], q_rot[i]])
-        s = keys[:, i, :] @ q * scale
+        s = keys @ q * scale
         m = s.max()
         e = np.exp(s - m)
         l = e.sum()
         a = e / l
-        o[i] = a @ values[:, i, :]
+        o[i] = a @ values
         o_lat[i] = a @ rows[:, :d_c]
         lse[i] = m + math.log(l)
         a_all[i] = a
