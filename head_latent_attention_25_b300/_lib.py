@@ -48,13 +48,13 @@ def load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     D = ctypes.POINTER(MlaDims)
-    lib.mla_cache_append.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P, P, P]
+    lib.mla_cache_append.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P, I64, P, P]
     lib.mla_cache_append.restype = I32
     lib.mla_project_query.argtypes = [D, I32, I32, I32, P, P, P, P, P, P]
     lib.mla_project_query.restype = I32
     lib.mla_decode_workspace_size.argtypes = [D, I32, I32, I32, I32]
     lib.mla_decode_workspace_size.restype = SZ
-    lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, P, P, I32, I32, P, SZ, P, P, P, P]
+    lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
     lib.mla_decode_absorbed.restype = I32
     lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P]
     lib.mla_project_out.restype = I32
@@ -102,10 +102,10 @@ def make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base=10000.0, softmax_scale=0
 
 
 def mla_cache_append(dims, dtype, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cache,
-                     dev_status, stream=None):
+                     cache_rows, dev_status, stream=None):
     _check("mla_cache_append", load().mla_cache_append(
         ctypes.byref(dims), dtype, batch, n_new, _p(h), _p(w_dkv), _p(w_kr), _p(row_off), _p(cap),
-        _p(pos0), _p(cache), _p(dev_status), _stream(stream)))
+        _p(pos0), _p(cache), cache_rows, _p(dev_status), _stream(stream)))
 
 
 def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, stream=None):
@@ -119,12 +119,13 @@ def mla_decode_workspace_size(dims, dtype, batch, max_seq_len, num_splits=0) -> 
                                                 num_splits))
 
 
-def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, row_off, seq_len, max_seq_len,
-                        num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream=None):
+def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len,
+                        max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                        stream=None):
     _check("mla_decode_absorbed", load().mla_decode_absorbed(
-        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), _p(row_off),
-        _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes, _p(o_lat), _p(lse),
-        _p(dev_status), _stream(stream)))
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
+        _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
 
 
 def mla_project_out(dims, dtype, batch, o_lat, w_uv, out, stream=None):

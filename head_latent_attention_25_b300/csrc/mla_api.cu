@@ -2,6 +2,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <climits>
 
 #include "mla_common.cuh"
 #include "mla_internal.h"
@@ -64,28 +65,41 @@ int sm_count() {
     return n;
 }
 
+// The tcgen05 kernel is written for the DeepSeek latent shape: 512 latent + 64 rotary
+// columns, at most 128 heads (one MMA M tile) and a cache of at least one 32-row tile.
+bool tc_shape(const mla_dims* d, mla_dtype t) {
+    return t == MLA_BF16 && d->d_c == 512 && d->d_r == 64 && d->n_heads <= 128;
+}
+
 struct DecodePlan {
+    bool tc;
     int workers;
+    int64_t q_rows;                  // rows of the folded-query buffer
     DecodeWorkspace ws;
 };
 
 bool plan_decode(const mla_dims* d, mla_dtype t, int batch, int max_seq_len, int num_splits,
-                 DecodePlan* p) {
+                 bool tc, DecodePlan* p) {
     if (!dims_ok(d) || !dtype_ok(t) || batch < 1 || max_seq_len < 0 || num_splits < 0) return false;
-    if (!simt_supported(d)) return false;
+    if (!tc && !simt_supported(d)) return false;
+    const int64_t rows_bound = (int64_t)batch * (max_seq_len > 0 ? max_seq_len : 1);
     int w = num_splits;
     if (w == 0) {
         const int sms = sm_count();
         if (sms <= 0) return false;
-        w = simt_workers(batch, d->n_heads, (int64_t)batch * (max_seq_len > 0 ? max_seq_len : 1), sms);
+        w = tc ? tc_workers(rows_bound, sms) : simt_workers(batch, d->n_heads, rows_bound, sms);
     }
     if (w > (1 << 20)) return false;
+    p->tc = tc;
     p->workers = w;
     DecodeWorkspace& ws = p->ws;
     const size_t A = 256;
     const int dq = d->d_c + d->d_r;
+    p->q_rows = (int64_t)batch * d->n_heads;
+    if (tc && p->q_rows < 128) p->q_rows = 128;      // one full 128-row TMA box always fits
     size_t off = 0;
-    ws.q_off = off;     ws.q_bytes = (size_t)batch * d->n_heads * dq * sizeof(float);
+    ws.q_off = off;
+    ws.q_bytes = (size_t)p->q_rows * dq * (tc ? 2 : sizeof(float));
     off = align_up(off + ws.q_bytes, A);
     ws.cum_off = off;   ws.cum_bytes = (size_t)(batch + 1) * sizeof(int64_t);
     off = align_up(off + ws.cum_bytes, A);
@@ -128,15 +142,17 @@ mla_status mla_profile_events(void* start, void* stop) {
 mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
                             const void* h, const void* w_dkv, const void* w_kr,
                             const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
-                            void* cache, int32_t* dev_status, void* stream) {
+                            void* cache, int64_t cache_rows, int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
-    if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30) || cache_rows < 1)
+        return MLA_ERR_INVALID_ARG;
     if (!h || !w_dkv || !w_kr || !row_off || !cap || !pos0 || !cache || !dev_status)
         return MLA_ERR_INVALID_ARG;
     const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
     return cuda_status(launch_append(*dims, dtype == MLA_BF16, batch, n_new, h, w_dkv, w_kr,
-                                     row_off, cap, pos0, cache, dev_status, (cudaStream_t)stream));
+                                     row_off, cap, pos0, cache, cache_rows, dev_status,
+                                     (cudaStream_t)stream));
 }
 
 mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
@@ -151,45 +167,57 @@ mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batc
 
 size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
                                  int32_t max_seq_len, int32_t num_splits) {
+    // bf16 latent-shape calls use the tensor-core kernel unless the cache is smaller
+    // than one tile, so size for whichever of the two kernels needs more.
     DecodePlan p;
-    if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, &p)) return 0;
-    return p.ws.total;
+    size_t need = 0;
+    if (plan_decode(dims, dtype, batch, max_seq_len, num_splits, false, &p)) need = p.ws.total;
+    if (dims_ok(dims) && dtype_ok(dtype) && tc_shape(dims, dtype) &&
+        plan_decode(dims, dtype, batch, max_seq_len, num_splits, true, &p) && p.ws.total > need)
+        need = p.ws.total;
+    return need;
 }
 
 mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
                                const void* q_c, const void* q_r, const void* w_uk,
-                               const void* cache, const int64_t* row_off, const int32_t* seq_len,
-                               int32_t max_seq_len, int32_t num_splits, void* workspace,
-                               size_t workspace_bytes, void* o_lat, float* lse,
+                               const void* cache, int64_t cache_rows, const int64_t* row_off,
+                               const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                                int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
-    if (batch < 1 || max_seq_len < 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || max_seq_len < 0 || num_splits < 0 || cache_rows < 1) return MLA_ERR_INVALID_ARG;
     if (!q_c || !q_r || !w_uk || !cache || !row_off || !seq_len || !o_lat || !dev_status)
         return MLA_ERR_INVALID_ARG;
     const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
-    if (!simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
+    const bool tc = tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
+    if (!tc && !simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
     DecodePlan p;
-    if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, &p)) return MLA_ERR_CUDA;
+    if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, tc, &p)) return MLA_ERR_CUDA;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < p.ws.total)
         return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)workspace;
-    float* qp = (float*)(ws + p.ws.q_off);
+    void* qp = ws + p.ws.q_off;
     int64_t* cum = (int64_t*)(ws + p.ws.cum_off);
     void* sched = ws + p.ws.sched_off;
     float* part_o = (float*)(ws + p.ws.po_off);
     float* part_l = (float*)(ws + p.ws.pl_off);
     const bool bf16 = dtype == MLA_BF16;
     const float alpha = scale_of(dims) * kLog2e;
-    cudaError_t e = launch_fold(*dims, bf16, false, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
-    if (e == cudaSuccess) e = launch_schedule(seq_len, batch, p.workers, cum, sched, s);
+    cudaError_t e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
     if (e == cudaSuccess)
-        e = launch_split_simt(*dims, bf16, batch, p.workers, qp, cache, row_off, seq_len, cum,
-                              sched, o_lat, lse, part_o, part_l, s);
+        e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, dev_status, s);
+    if (e == cudaSuccess) {
+        if (tc)
+            e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cache, cache_rows, row_off, cum,
+                                sched, o_lat, lse, part_o, part_l, dev_status, s);
+        else
+            e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
+                                  sched, o_lat, lse, part_o, part_l, s);
+    }
     if (e == cudaSuccess)
-        e = launch_merge(*dims, bf16, batch, seq_len, cum, sched, part_o, part_l, o_lat, lse,
-                         dev_status, s);
+        e = launch_merge(*dims, bf16, batch, cum, sched, part_o, part_l, o_lat, lse, s);
     return cuda_status(e);
 }
 

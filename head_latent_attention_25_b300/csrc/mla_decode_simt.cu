@@ -15,9 +15,12 @@ namespace mla {
 namespace {
 
 // ------------------------------------------------------------------ schedule
-__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len, int batch,
-                                                        int workers, int64_t* cum,
-                                                        Schedule* sched) {
+// A sequence takes part with its length when 1 <= seq_len and its rows lie inside the
+// cache buffer; otherwise it counts as empty and MLA_DEV_BAD_LENGTH is raised.
+__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len,
+                                                        const int64_t* row_off, int64_t cache_rows,
+                                                        int batch, int workers, int64_t* cum,
+                                                        Schedule* sched, int32_t* dev_status) {
     __shared__ long long warp_tot[32];
     __shared__ long long carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -25,7 +28,12 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len, 
     __syncthreads();
     for (int base = 0; base < batch; base += 1024) {
         const int i = base + tid;
-        long long x = (i < batch) ? (long long)max(seq_len[i], 0) : 0;
+        long long x = 0;
+        if (i < batch) {
+            const long long n = seq_len[i], o = row_off[i];
+            if (n >= 1 && o >= 0 && o + n <= cache_rows) x = n;
+            else atomicOr(dev_status, MLA_DEV_BAD_LENGTH);
+        }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             long long y = __shfl_up_sync(0xffffffffu, x, o);
@@ -175,19 +183,15 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
 
 // ------------------------------------------------------------------ merge
 template <typename Tout>
-__global__ void __launch_bounds__(128) merge_kernel(const int32_t* seq_len, const int64_t* cum,
-                                                    const Schedule* sched, const float* part_o,
-                                                    const float* part_l, Tout* o_lat, float* lse,
-                                                    int32_t* dev_status, int n_h, int d_c) {
+__global__ void __launch_bounds__(128) merge_kernel(const int64_t* cum, const Schedule* sched,
+                                                    const float* part_o, const float* part_l,
+                                                    Tout* o_lat, float* lse, int n_h, int d_c) {
     const int bh = blockIdx.x;
     const int b = bh / n_h, h = bh - b * n_h;
     Tout* out = o_lat + (int64_t)bh * d_c;
-    if (seq_len[b] < 1) {
+    if (cum[b + 1] == cum[b]) {                 // empty or rejected by the schedule
         for (int c = threadIdx.x; c < d_c; c += blockDim.x) st(out + c, 0.f);
-        if (threadIdx.x == 0) {
-            if (lse) lse[bh] = -INFINITY;
-            if (h == 0) atomicOr(dev_status, MLA_DEV_BAD_LENGTH);
-        }
+        if (threadIdx.x == 0 && lse) lse[bh] = -INFINITY;
         return;
     }
     const int64_t per = sched->per;
@@ -217,9 +221,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const int32_t* seq_len, cons
 
 }  // namespace
 
-cudaError_t launch_schedule(const int32_t* seq_len, int batch, int workers, int64_t* cum,
-                            void* sched, cudaStream_t s) {
-    schedule_kernel<<<1, 1024, 0, s>>>(seq_len, batch, workers, cum, (Schedule*)sched);
+cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
+                            int batch, int workers, int64_t* cum, void* sched, int32_t* dev_status,
+                            cudaStream_t s) {
+    schedule_kernel<<<1, 1024, 0, s>>>(seq_len, row_off, cache_rows, batch, workers, cum,
+                                       (Schedule*)sched, dev_status);
     note_launch();
     return cudaGetLastError();
 }
@@ -235,10 +241,9 @@ int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count) {
 }
 
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
-                              const void* cache, const int64_t* row_off, const int32_t* seq_len,
-                              const int64_t* cum, const void* sched, void* o_lat, float* lse,
-                              float* part_o, float* part_l, cudaStream_t s) {
-    (void)seq_len;
+                              const void* cache, const int64_t* row_off, const int64_t* cum,
+                              const void* sched, void* o_lat, float* lse, float* part_o,
+                              float* part_l, cudaStream_t s) {
     SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, o_lat, lse, part_o, part_l,
                 d.n_heads, d.d_c, d.d_r, batch};
     const int dq = d.d_c + d.d_r;
@@ -263,17 +268,16 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int32_t* seq_len,
-                         const int64_t* cum, const void* sched, const float* part_o,
-                         const float* part_l, void* o_lat, float* lse, int32_t* dev_status,
-                         cudaStream_t s) {
+cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
+                         const void* sched, const float* part_o, const float* part_l, void* o_lat,
+                         float* lse, cudaStream_t s) {
     const int blocks = batch * d.n_heads;
     if (bf16)
-        merge_kernel<<<blocks, 128, 0, s>>>(seq_len, cum, (const Schedule*)sched, part_o, part_l,
-                                            (__nv_bfloat16*)o_lat, lse, dev_status, d.n_heads, d.d_c);
+        merge_kernel<<<blocks, 128, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                            (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
     else
-        merge_kernel<<<blocks, 128, 0, s>>>(seq_len, cum, (const Schedule*)sched, part_o, part_l,
-                                            (float*)o_lat, lse, dev_status, d.n_heads, d.d_c);
+        merge_kernel<<<blocks, 128, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                            (float*)o_lat, lse, d.n_heads, d.d_c);
     note_launch();
     return cudaGetLastError();
 }

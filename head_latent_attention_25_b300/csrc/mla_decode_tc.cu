@@ -1,0 +1,518 @@
+// Split-K absorbed decode on tcgen05 tensor cores (sm_103a), bf16 latent cache with
+// d_c = 512, d_r = 64 and up to 128 heads.
+//
+// Work unit: a 2-CTA cluster walks one contiguous range of the flattened context
+// (same schedule as the CUDA-core kernel).  CTA r of the pair owns latent columns
+// [256r, 256r+256) and rotary columns [512+32r, 512+32r+32) of every cache row, so
+// the pair streams each row from HBM exactly once.  Per tile of 32 rows:
+//
+//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=32 rows, K=288 (smem x smem -> TMEM)
+//   S   = S_0 + S_1          each CTA sends its fp32 partial to the peer through DSMEM
+//   P   = exp2(S - m)        online softmax (identical in both CTAs; lazy max update)
+//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=32 (cache tile as MN-major B)
+//
+// O_r (128 x 256 fp32) lives in TMEM for the whole range; S is double buffered in
+// TMEM.  Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
+// warps 4-7 softmax/exchange/epilogue (thread i <-> head i <-> TMEM lane i).
+// Every wait is bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains
+// its own in-flight copies and MMAs, frees TMEM and returns.
+#include <mutex>
+
+#include "mla_common.cuh"
+#include "mla_internal.h"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kTok = 32;              // cache rows per tile
+constexpr int kStages = 4;            // TMA ring depth
+constexpr int kThreads = 256;
+constexpr int kHeads = 128;           // MMA M (heads beyond n_heads are computed and dropped)
+constexpr int kLatHalf = 256;         // latent columns per CTA
+constexpr int kRopeHalf = 32;         // rotary columns per CTA
+constexpr int kRowElems = 576;        // d_c + d_r
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// shared memory layout (byte offsets from a 1024-aligned base)
+constexpr uint32_t kQBox = kHeads * 128;                 // 128 rows x 64 bf16, 128B swizzle
+constexpr uint32_t kQRope = kHeads * 64;                 // 128 rows x 32 bf16, 64B swizzle
+constexpr uint32_t kQBytes = 4 * kQBox + kQRope;         // 73728
+constexpr uint32_t kTBox = kTok * 128;                   // 32 rows x 64 bf16
+constexpr uint32_t kTRope = kTok * 64;                   // 32 rows x 32 bf16
+constexpr uint32_t kStageBytes = 4 * kTBox + kTRope;     // 18432
+constexpr uint32_t kPBytes = kHeads * kTok * 2;          // P tile, bf16, 64B swizzle
+constexpr uint32_t kXBytes = kHeads * kTok * 4;          // peer's fp32 partial scores
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffStage = kOffQ + kQBytes;
+constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;
+constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffBar = kOffX + 2 * kXBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers/flags + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// barrier indices
+enum : int {
+    B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
+    B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2, B_ODONE = B_PEMPTY + 2,
+    B_OFREE, B_XFULL, B_XEMPTY = B_XFULL + 2, B_FIN = B_XEMPTY + 2, B_COUNT
+};
+static_assert(B_COUNT * 8 <= 200, "barrier area");
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;          // O_r: 256 columns
+constexpr uint32_t kColS = 256;        // S: 2 x 32 columns
+
+struct TcArgs {
+    const int64_t* row_off;
+    const int64_t* cum;
+    const Schedule* sched;
+    __nv_bfloat16* o_lat;
+    float* lse;
+    float* part_o;
+    float* part_l;
+    int32_t* dev_status;
+    int n_h;
+    int batch;
+};
+
+struct Seg {
+    int b;
+    int64_t lo, hi, len;
+    bool complete;
+    int64_t slot;
+};
+
+// Walks the sequences that a worker's range [g*per, (g+1)*per) of the flattened
+// context touches (identical in every role of both CTAs).
+struct SegWalk {
+    const int64_t* cum;
+    int64_t cur, end;
+    int b, g;
+    bool first;
+    __device__ void init(const int64_t* c, int batch, int gi, int64_t per, int64_t total) {
+        cum = c;
+        g = gi;
+        cur = (int64_t)gi * per;
+        end = min(cur + per, total);
+        first = true;
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] <= cur) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+    }
+    __device__ bool next(Seg& s) {
+        if (cur >= end) return false;
+        while (cum[b + 1] <= cur) ++b;
+        const int64_t seq0 = cum[b];
+        s.b = b;
+        s.len = cum[b + 1] - seq0;
+        s.lo = cur - seq0;
+        s.hi = min(s.len, end - seq0);
+        s.complete = (s.lo == 0 && s.hi == s.len);
+        s.slot = 2 * (int64_t)g + (first ? 0 : 1);
+        cur = seq0 + s.hi;
+        first = false;
+        return true;
+    }
+};
+
+struct Ctl {
+    volatile int* abort;
+    int32_t* dev_status;
+};
+
+// Bounded wait: true when the phase completed; false on abort or time-out (which
+// also raises the abort flag and MLA_DEV_TIMEOUT).
+template <bool kCluster>
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *c.abort = 1;
+            atomicOr(c.dev_status, MLA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Warp-uniform form for the softmax warps: tcgen05.ld/st and warp votes need all 32
+// lanes on the same path, so a lane that gives up makes the whole warp give up.
+template <bool kCluster>
+__device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, const Ctl& c) {
+    const bool ok = wait<kCluster>(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used while draining after an abort: ignores the abort flag, bounded in time.
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kTimeoutNs) return;
+}
+
+__device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return smem_desc(a, 16, 1024, kSwizzle128B); }
+__device__ __forceinline__ uint64_t kdesc64(uint32_t a) { return smem_desc(a, 16, 512, kSwizzle64B); }
+// MN-major 128B-swizzled B: 64-column atoms 4096 B apart (one TMA box), 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return smem_desc(a, kTBox, 1024, kSwizzle128B); }
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
+                const __grid_constant__ CUtensorMap map_q128, const __grid_constant__ CUtensorMap map_q64,
+                TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Schedule S = *a.sched;
+    const int g = blockIdx.x >> 1;
+    if ((int64_t)g * S.per >= S.total) return;          // both CTAs of the pair leave together
+
+    const uint32_t base = smem_addr(sm);
+    const uint32_t sQ = base + kOffQ, sStage = base + kOffStage, sP = base + kOffP, sX = base + kOffX;
+    uint64_t* bars = (uint64_t*)(sm + kOffBar);
+    uint32_t* tslot = (uint32_t*)(sm + kOffBar + 200);
+    volatile int* abort_flag = (volatile int*)(sm + kOffBar + 204);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    Ctl ctl{abort_flag, a.dev_status};
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
+        mbar_init(bar(B_QFULL), 1);
+        mbar_init(bar(B_QEMPTY), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_SFULL + i), 1);
+            mbar_init(bar(B_SEMPTY + i), 128);
+            mbar_init(bar(B_PFULL + i), 128);
+            mbar_init(bar(B_PEMPTY + i), 1);
+            mbar_init(bar(B_XFULL + i), 128);
+            mbar_init(bar(B_XEMPTY + i), 128);
+        }
+        mbar_init(bar(B_ODONE), 1);
+        mbar_init(bar(B_OFREE), 128);
+        mbar_init(bar(B_FIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init_cluster();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_addr(tslot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&map_c128); prefetch_tmap(&map_c64);
+        prefetch_tmap(&map_q128); prefetch_tmap(&map_q64);
+    }
+    tc_fence_before();
+    cluster_sync();                 // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    SegWalk walk;
+    walk.init(a.cum, a.batch, g, S.per, S.total);
+    Seg seg;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t T = 0, si = 0;
+            bool ok = true;
+            while (ok && walk.next(seg)) {
+                ok = wait<false>(bar(B_QEMPTY), (si & 1) ^ 1, ctl);
+                if (!ok) break;
+                mbar_expect_tx(bar(B_QFULL), kQBytes);
+                const int qy = seg.b * a.n_h;
+                for (int j = 0; j < 4; ++j)
+                    tma_load_2d(sQ + j * kQBox, &map_q128, rank * kLatHalf + 64 * j, qy, bar(B_QFULL));
+                tma_load_2d(sQ + 4 * kQBox, &map_q64, 512 + rank * kRopeHalf, qy, bar(B_QFULL));
+                const int64_t row0 = a.row_off[seg.b] + seg.lo;
+                const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
+                for (int t = 0; t < ntiles; ++t, ++T) {
+                    const uint32_t st = T % kStages;
+                    ok = wait<false>(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1, ctl);
+                    if (!ok) break;
+                    const uint32_t dst = sStage + st * kStageBytes;
+                    const int y = (int)(row0 + (int64_t)t * kTok);
+                    mbar_expect_tx(bar(B_FULL + st), kStageBytes);
+                    for (int j = 0; j < 4; ++j)
+                        tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
+                    tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
+                }
+                ++si;
+            }
+            // drain: every copy this thread issued has landed before the CTA may exit
+            for (uint32_t k = 0; k < kStages && k < T; ++k) {
+                const uint32_t Tk = T - 1 - k;
+                drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
+            }
+            if (si > 0) drain(bar(B_QFULL), (si - 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
+            const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
+            uint32_t T = 0, si = 0;
+            bool ok = true;
+            bool have_prev = false;
+            uint32_t pT = 0, pSeg = 0;
+            bool pFirst = false;
+            auto issue_pv = [&](uint32_t Tp, uint32_t segp, bool firstp) -> bool {
+                const uint32_t sb = Tp & 1, st = Tp % kStages;
+                if (!wait<false>(bar(B_PFULL + sb), (Tp >> 1) & 1, ctl)) return false;
+                if (firstp && segp > 0 && !wait<false>(bar(B_OFREE), (segp - 1) & 1, ctl)) return false;
+                tc_fence_after();
+                const uint32_t stage = sStage + st * kStageBytes;
+                for (int k = 0; k < kTok / 16; ++k)
+                    mma_bf16(tmem + kColO, kdesc64(sP + sb * kPBytes + 32 * k),
+                             mndesc128(stage + 2048 * k), id_o, (firstp && k == 0) ? 0u : 1u);
+                mma_commit(bar(B_EMPTY + st));
+                mma_commit(bar(B_PEMPTY + sb));
+                mma_commit(bar(B_ODONE));
+                return true;
+            };
+            while (ok && walk.next(seg)) {
+                ok = wait<false>(bar(B_QFULL), si & 1, ctl);
+                if (!ok) break;
+                const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
+                for (int t = 0; t < ntiles && ok; ++t, ++T) {
+                    const uint32_t st = T % kStages, sb = T & 1;
+                    ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl) &&
+                         wait<false>(bar(B_SEMPTY + sb), ((T >> 1) & 1) ^ 1, ctl);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t stage = sStage + st * kStageBytes;
+                    const uint32_t d = tmem + kColS + sb * kTok;
+                    for (int j = 0; j < 4; ++j)
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(d, kdesc128(sQ + j * kQBox + 32 * k), kdesc128(stage + j * kTBox + 32 * k),
+                                     id_s, (j | k) ? 1u : 0u);
+                    for (int k = 0; k < 2; ++k)
+                        mma_bf16(d, kdesc64(sQ + 4 * kQBox + 32 * k), kdesc64(stage + 4 * kTBox + 32 * k),
+                                 id_s, 1u);
+                    mma_commit(bar(B_SFULL + sb));
+                    if (t == ntiles - 1) mma_commit(bar(B_QEMPTY));
+                    if (have_prev) ok = issue_pv(pT, pSeg, pFirst);
+                    have_prev = true;
+                    pT = T; pSeg = si; pFirst = (t == 0);
+                }
+                ++si;
+            }
+            if (ok && have_prev) issue_pv(pT, pSeg, pFirst);
+            mma_commit(bar(B_FIN));
+            drain(bar(B_FIN), 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax / exchange / epilogue
+        const int i = tid - 128;                        // head row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t peer_x = mapa(sX, peer);
+        const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
+        const uint32_t peer_xempty = mapa(bar(B_XEMPTY), peer);
+        const uint32_t xrow = (uint32_t)i * (kTok * 4);   // this row's 128 bytes in an X buffer
+        uint32_t T = 0, si = 0;
+        bool ok = true;
+        while (ok && walk.next(seg)) {
+            float m_run = -INFINITY, l_run = 0.f;
+            const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
+            for (int t = 0; t < ntiles; ++t, ++T) {
+                const uint32_t sb = T & 1, par = (T >> 1) & 1, st = T % kStages;
+                float s[kTok];
+                if (!(ok = wwait<false>(bar(B_SFULL + sb), par, ctl))) break;
+                tc_fence_after();
+                tmem_ld32(tmem + lane_base + kColS + sb * kTok, s);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(B_SEMPTY + sb));
+                // send my partial scores into the peer's X buffer, then take the peer's
+                if (!(ok = wwait<true>(bar(B_XEMPTY + sb), par ^ 1, ctl))) break;
+                for (int c = 0; c < kTok / 4; ++c) {
+                    const uint32_t off = xrow + (uint32_t)((c ^ (i & 7)) * 16);
+                    st_cluster_v4(peer_x + sb * kXBytes + off, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                }
+                mbar_arrive_remote(peer_xfull + 8 * sb);
+                if (!(ok = wwait<true>(bar(B_XFULL + sb), par, ctl))) break;
+                const uint8_t* xb = sm + kOffX + sb * kXBytes + xrow;
+                for (int c = 0; c < kTok / 4; ++c) {
+                    const float4 v = *(const float4*)(xb + ((c ^ (i & 7)) * 16));
+                    s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
+                }
+                mbar_arrive_remote(peer_xempty + 8 * sb);
+                // rows past the end of this piece do not count
+                const int valid = (int)min((int64_t)kTok, seg.hi - seg.lo - (int64_t)t * kTok);
+                float mt = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) {
+                    if (j >= valid) s[j] = -INFINITY;
+                    mt = fmaxf(mt, s[j]);
+                }
+                // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
+                const bool need = mt > m_run + 8.f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = exp2f(m_run - mt);
+                    m_run = mt;
+                    l_run *= alpha;
+                }
+                if (t > 0 && __any_sync(0xffffffffu, need)) {
+                    if (!(ok = wwait<false>(bar(B_ODONE), (T - 1) & 1, ctl))) break;
+                    tc_fence_after();
+                    for (int c = 0; c < kLatHalf / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                        tmem_st32(tmem + lane_base + kColO + 32 * c, o);
+                    }
+                    tmem_wait_st();
+                }
+                // P tile (bf16) for the value MMA; the sum uses the rounded values
+                if (!(ok = wwait<false>(bar(B_PEMPTY + sb), par ^ 1, ctl))) break;
+                uint32_t packed[kTok / 2];
+#pragma unroll
+                for (int j = 0; j < kTok / 2; ++j) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_run), exp2f(s[2 * j + 1] - m_run));
+                    l_run += __low2float(h2) + __high2float(h2);
+                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                uint8_t* prow = sm + kOffP + sb * kPBytes + i * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *(uint4*)(prow + ((c ^ ((i >> 1) & 3)) * 16)) =
+                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                if (valid < kTok) {
+                    // the value MMA must not see rows of the tile beyond the piece (they may
+                    // hold anything): zero them in this CTA's latent half of the stage
+                    uint8_t* stage = sm + kOffStage + st * kStageBytes;
+                    for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
+                        const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
+                        *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(B_PFULL + sb));
+            }
+            if (!ok) break;
+            // epilogue of this piece: O_r / l, log2-sum-exp
+            if (!(ok = wwait<false>(bar(B_ODONE), (T - 1) & 1, ctl))) break;
+            tc_fence_after();
+            const float inv = 1.f / l_run;
+            const float lse2 = m_run + log2f(l_run);
+            const bool row_ok = i < a.n_h;
+            for (int c = 0; c < kLatHalf / 32; ++c) {
+                float o[32];
+                tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                const int col = (int)rank * kLatHalf + 32 * c;
+                if (seg.complete) {
+                    __nv_bfloat16* dst = a.o_lat + ((int64_t)seg.b * a.n_h + i) * 512 + col;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * q + 2 * e] * inv, o[8 * q + 2 * e + 1] * inv);
+                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        *(uint4*)(dst + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float* dst = a.part_o + (seg.slot * a.n_h + i) * 512 + col;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *(float4*)(dst + 4 * q) = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
+                                                              o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+                }
+            }
+            if (row_ok && rank == 0) {
+                if (seg.complete) { if (a.lse) a.lse[(int64_t)seg.b * a.n_h + i] = lse2 * kLn2; }
+                else a.part_l[seg.slot * a.n_h + i] = lse2;
+            }
+            tc_fence_before();
+            mbar_arrive(bar(B_OFREE));
+            ++si;
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    cluster_sync();                 // the peer no longer writes into this CTA's shared memory
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    });
+    return g_encode != nullptr;
+}
+
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
+               CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {bx, by};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_workers(int64_t max_total_rows, int sm_count) {
+    int64_t w = sm_count / 2;                           // one 2-CTA cluster per SM pair
+    const int64_t by_rows = (max_total_rows + 4 * kTok - 1) / (4 * kTok);
+    if (w > by_rows) w = by_rows;
+    if (w < 1) w = 1;
+    return (int)w;
+}
+
+cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
+                            int64_t q_rows, const void* cache, int64_t cache_rows,
+                            const int64_t* row_off, const int64_t* cum, const void* sched,
+                            void* o_lat, float* lse, float* part_o, float* part_l,
+                            int32_t* dev_status, cudaStream_t s) {
+    if (!get_encoder()) return cudaErrorNotSupported;
+    CUtensorMap mc128, mc64, mq128, mq64;
+    if (!encode_2d(&mc128, cache, kRowElems, (uint64_t)cache_rows, 64, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !encode_2d(&mq128, qp, kRowElems, (uint64_t)q_rows, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mq64, qp, kRowElems, (uint64_t)q_rows, 32, kHeads, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    TcArgs a{row_off, cum, (const Schedule*)sched, (__nv_bfloat16*)o_lat, lse, part_o, part_l, dev_status,
+             d.n_heads, batch};
+    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    profile_before_split(s);
+    split_tc_kernel<<<dim3(2 * workers), dim3(kThreads), kSmemBytes, s>>>(mc128, mc64, mq128, mq64, a);
+    profile_after_split(s);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -12,8 +12,8 @@ struct DecodeWorkspace;
 
 cudaError_t launch_append(const mla_dims& d, bool bf16, int batch, int n_new, const void* h,
                           const void* w_dkv, const void* w_kr, const int64_t* row_off,
-                          const int32_t* cap, const int32_t* pos0, void* cache, int32_t* dev_status,
-                          cudaStream_t s);
+                          const int32_t* cap, const int32_t* pos0, void* cache, int64_t cache_rows,
+                          int32_t* dev_status, cudaStream_t s);
 
 cudaError_t launch_project_query(const mla_dims& d, bool bf16, int batch, int d_in, const void* x,
                                  const void* w_uq, const void* w_qr, void* q_c, void* q_r,
@@ -27,21 +27,29 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
 cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const void* o_lat,
                                const void* w_uv, void* out, cudaStream_t s);
 
-// Work split of the flattened context: prefix sums + Schedule into the workspace.
-cudaError_t launch_schedule(const int32_t* seq_len, int batch, int workers, int64_t* cum,
-                            void* sched, cudaStream_t s);
+// Work split of the flattened context: prefix sums of the usable sequence lengths and
+// the Schedule, written into the workspace; flags unusable sequences.
+cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
+                            int batch, int workers, int64_t* cum, void* sched, int32_t* dev_status,
+                            cudaStream_t s);
 
 // fp32-Q' SIMT split kernel (any supported dims, fp32 or bf16 cache).
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
-                              const void* cache, const int64_t* row_off, const int32_t* seq_len,
-                              const int64_t* cum, const void* sched, void* o_lat, float* lse,
-                              float* part_o, float* part_l, cudaStream_t s);
+                              const void* cache, const int64_t* row_off, const int64_t* cum,
+                              const void* sched, void* o_lat, float* lse, float* part_o,
+                              float* part_l, cudaStream_t s);
 
-// Combines the partial results of sequences cut across workers; flags empty sequences.
-cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int32_t* seq_len,
-                         const int64_t* cum, const void* sched, const float* part_o,
-                         const float* part_l, void* o_lat, float* lse, int32_t* dev_status,
-                         cudaStream_t s);
+// bf16 tcgen05 split kernel for d_c = 512, d_r = 64, n_heads <= 128 (2-CTA clusters).
+cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
+                            int64_t q_rows, const void* cache, int64_t cache_rows,
+                            const int64_t* row_off, const int64_t* cum, const void* sched,
+                            void* o_lat, float* lse, float* part_o, float* part_l,
+                            int32_t* dev_status, cudaStream_t s);
+
+// Combines the partial results of sequences cut across workers; zero-fills empty ones.
+cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
+                         const void* sched, const float* part_o, const float* part_l, void* o_lat,
+                         float* lse, cudaStream_t s);
 
 // Launch accounting and the optional per-thread timing hook around the split kernel.
 void note_launch(int n = 1);
@@ -49,5 +57,6 @@ void profile_before_split(cudaStream_t s);
 void profile_after_split(cudaStream_t s);
 
 int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count);
+int tc_workers(int64_t max_total_rows, int sm_count);
 
 }  // namespace mla

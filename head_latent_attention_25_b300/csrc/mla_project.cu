@@ -25,6 +25,7 @@ struct GemmArgs {
     int32_t n_new, d_c, d_r;
     float rope_base;
     const int64_t* row_off; const int32_t* cap; const int32_t* pos0; int32_t* dev_status;
+    int64_t cache_rows;
 };
 
 template <typename Tin, typename Tout>
@@ -86,13 +87,14 @@ __global__ void __launch_bounds__(NT) gemm_xwt_kernel(GemmArgs a) {
         } else {
             const int b = m / a.n_new, t = m % a.n_new;
             const int p0 = a.pos0[b];
-            if (p0 < 0 || (int64_t)p0 + a.n_new > (int64_t)a.cap[b]) {
+            const int64_t off = a.row_off[b], cap = a.cap[b];
+            if (p0 < 0 || (int64_t)p0 + a.n_new > cap || off < 0 || off + cap > a.cache_rows) {
                 if (t == 0 && n == 0) atomicOr(a.dev_status, MLA_DEV_BAD_POSITION);
                 continue;
             }
             const int64_t pos = (int64_t)p0 + t;
             const int row_elems = a.d_c + a.d_r;
-            Tout* Y = (Tout*)a.y + (a.row_off[b] + pos) * row_elems + n;
+            Tout* Y = (Tout*)a.y + (off + pos) * row_elems + n;
             if (n >= a.d_c) {            // k_R = RoPE(W_KR h, pos) on the pair (2k, 2k+1)
                 float c, s;
                 rope_cos_sin(pos, (n - a.d_c) >> 1, a.d_r, a.rope_base, &c, &s);
@@ -154,9 +156,10 @@ __global__ void fold_rope_kernel(const Tin* q_r, const int32_t* seq_len, Tout* q
 
 cudaError_t launch_append(const mla_dims& d, bool bf16, int batch, int n_new, const void* h,
                           const void* w_dkv, const void* w_kr, const int64_t* row_off,
-                          const int32_t* cap, const int32_t* pos0, void* cache, int32_t* dev_status,
-                          cudaStream_t s) {
+                          const int32_t* cap, const int32_t* pos0, void* cache, int64_t cache_rows,
+                          int32_t* dev_status, cudaStream_t s) {
     GemmArgs a = blank();
+    a.cache_rows = cache_rows;
     a.x = h; a.x_g = 0; a.x_m = d.hidden;
     a.w = w_dkv; a.w2 = w_kr; a.n_split = d.d_c;
     a.w_g = 0; a.w_n = d.hidden; a.w_k = 1;

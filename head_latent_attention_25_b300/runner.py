@@ -87,7 +87,7 @@ class DecodeStep:
     def append(self, stream=None):
         L.mla_cache_append(self.dims, self.dt, self.batch, self.n_new, self.h, self.w["w_dkv"],
                            self.w["w_kr"], self.row_off, self.cap, self.pos0, self.cache,
-                           self.dev_status, stream)
+                           self.total_rows, self.dev_status, stream)
 
     def project_query(self, stream=None):
         L.mla_project_query(self.dims, self.dt, self.batch, self.d_q_in, self.x_q, self.w["w_uq"],
@@ -100,7 +100,8 @@ class DecodeStep:
             nb = L.mla_decode_workspace_size(self.dims, self.dt, self.batch, self.max_seq_len, ns)
             ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
         L.mla_decode_absorbed(self.dims, self.dt, self.batch, self.q_c, self.q_r, self.w["w_uk"],
-                              self.cache, self.row_off, self.seq_len, self.max_seq_len, ns, ws,
+                              self.cache, self.total_rows, self.row_off, self.seq_len,
+                              self.max_seq_len, ns, ws,
                               ws.numel(), self.o_lat if o_lat is None else o_lat,
                               self.lse if lse is None else lse, self.dev_status, stream)
 

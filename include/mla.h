@@ -96,14 +96,17 @@ typedef struct {
  *   pos0     [batch] int32            position of the first new token of each sequence
  *   cache    rows of d_c + d_r        token t of sequence b goes to row
  *                                     row_off[b] + pos0[b] + t, rotated at position pos0[b] + t
+ *   cache_rows                        rows in the cache buffer (host value, >= 1)
  *   dev_status int32 (device)         MLA_DEV_BAD_POSITION is OR-ed in for a sequence whose
- *                                     new rows would leave [0, cap[b]); its rows are skipped
+ *                                     new rows would leave [0, cap[b]) or the buffer
+ *                                     (row_off[b] < 0 or row_off[b] + cap[b] > cache_rows);
+ *                                     its rows are skipped
  * Row values are rounded once from the fp32 accumulator to `dtype`.
  */
 MLA_API mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
                             const void* h, const void* w_dkv, const void* w_kr,
                             const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
-                            void* cache, int32_t* dev_status, void* stream);
+                            void* cache, int64_t cache_rows, int32_t* dev_status, void* stream);
 
 /*
  * mla_project_query -- per-head query parts from a query input x (the query latent
@@ -137,7 +140,7 @@ MLA_API size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, 
  *   q_c      [batch, n_h, d_h]     content query
  *   q_r      [batch, n_h, d_r]     rotary query, not yet rotated
  *   w_uk     [n_h, d_h, d_c]       key up-projection
- *   cache, row_off                 as for mla_cache_append
+ *   cache, cache_rows, row_off     as for mla_cache_append
  *   seq_len  [batch] int32         rows of each sequence (new token included); the query
  *                                  sits at position seq_len[b]-1 and attends over rows
  *                                  0 .. seq_len[b]-1
@@ -149,14 +152,17 @@ MLA_API size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, 
  *                aligned; contents on entry are ignored
  *   o_lat    [batch, n_h, d_c]     out: sum_j a_ij c_j, in `dtype`
  *   lse      [batch, n_h] fp32     out (may be NULL): natural log of sum_j exp(s_ij)
- *   dev_status                     MLA_DEV_BAD_LENGTH for seq_len[b] < 1 (outputs of b
- *                                  zero, lse -inf); MLA_DEV_TIMEOUT if a bounded wait
- *                                  expired
+ *   dev_status                     MLA_DEV_BAD_LENGTH for seq_len[b] < 1 or rows outside
+ *                                  the buffer (row_off[b] < 0 or row_off[b] + seq_len[b] >
+ *                                  cache_rows): outputs of b zero, lse -inf;
+ *                                  MLA_DEV_TIMEOUT if a bounded wait expired
+ * bf16 with d_c = 512, d_r = 64, n_heads <= 128 and cache_rows >= 32 runs on the tcgen05
+ * tensor-core kernel; every other supported shape runs on CUDA cores.
  */
 MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
                                const void* q_c, const void* q_r, const void* w_uk,
-                               const void* cache, const int64_t* row_off, const int32_t* seq_len,
-                               int32_t max_seq_len, int32_t num_splits,
+                               const void* cache, int64_t cache_rows, const int64_t* row_off,
+                               const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
                                void* workspace, size_t workspace_bytes,
                                void* o_lat, float* lse, int32_t* dev_status, void* stream);
 

@@ -61,7 +61,8 @@ def test_small_bf16_split_count_invariance(num_splits):
     a, b = auto.o_lat.double(), st.o_lat.double()
     # o_lat is stored in bf16: allow two units in the last place of the largest value
     assert float((a - b).abs().max()) <= 2.0 ** -7 * float(a.abs().max())
-    assert float((auto.lse - st.lse).abs().max()) <= 1e-4
+    # lse: P is rounded to bf16 against a running maximum that depends on the split
+    assert float((auto.lse - st.lse).abs().max()) <= 1e-4 * float(auto.lse.abs().max()) + 1e-4
     _compare(st, wl, 5, what=f" splits={num_splits}")
 
 
@@ -151,13 +152,13 @@ def test_host_errors():
     wl = mla_inputs.WORKLOADS["small_bf16"]
     st = runner.from_workload(wl, load_inputs=False)
     with pytest.raises(L.MlaError) as e:
-        L.mla_decode_absorbed(st.dims, st.dt, st.batch, st.q_c, st.q_r, st.q_c, st.cache, st.row_off,
-                              st.seq_len, st.max_seq_len, 0, st.workspace, 64, st.o_lat, st.lse,
-                              st.dev_status)
+        L.mla_decode_absorbed(st.dims, st.dt, st.batch, st.q_c, st.q_r, st.q_c, st.cache, st.total_rows,
+                              st.row_off, st.seq_len, st.max_seq_len, 0, st.workspace, 64, st.o_lat,
+                              st.lse, st.dev_status)
     assert e.value.status == L.MLA_ERR_WORKSPACE
     big = L.make_dims(4, 16, 1024, 64, 64)
     with pytest.raises(L.MlaError) as e:
-        L.mla_decode_absorbed(big, st.dt, st.batch, st.q_c, st.q_r, st.q_c, st.cache, st.row_off,
-                              st.seq_len, st.max_seq_len, 0, st.workspace, st.ws_bytes, st.o_lat,
-                              st.lse, st.dev_status)
+        L.mla_decode_absorbed(big, st.dt, st.batch, st.q_c, st.q_r, st.q_c, st.cache, st.total_rows,
+                              st.row_off, st.seq_len, st.max_seq_len, 0, st.workspace, st.ws_bytes,
+                              st.o_lat, st.lse, st.dev_status)
     assert e.value.status == L.MLA_ERR_UNSUPPORTED
