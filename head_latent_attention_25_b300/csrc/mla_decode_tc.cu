@@ -11,9 +11,12 @@
 //   P   = exp2(S - m)        online softmax (identical in both CTAs; lazy max update)
 //   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=32 (cache tile as MN-major B)
 //
-// O_r (128 x 256 fp32) lives in TMEM for the whole range; S is double buffered in
-// TMEM.  Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM owner,
-// warps 4-7 softmax/exchange/epilogue (thread i <-> head i <-> TMEM lane i).
+// O_r (128 x 256 fp32) lives in TMEM for the whole range; four score tiles rotate
+// through TMEM.  Warp roles: warp 0 TMA producer, warp 1 MMA issuer (score MMAs two
+// tiles ahead of the value MMA), warp 2 TMEM owner, warps 4-7 softmax/exchange/
+// epilogue (thread i <-> head i <-> TMEM lane i), which fetch and send the next
+// tile's partial scores before working on the current one.  The exchange uses
+// st.async with the peer's mbarrier counting the bytes, so it needs no fences.
 // Every wait is bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains
 // its own in-flight copies and MMAs, frees TMEM and returns.
 #include <mutex>
@@ -31,6 +34,13 @@ using namespace tc;
 
 constexpr int kTok = 32;              // cache rows per tile
 constexpr int kStages = 4;            // TMA ring depth
+constexpr int kSBuf = 4;              // score tiles in TMEM (score MMA runs 2 tiles ahead)
+constexpr int kXBuf = 4;              // exchange buffers (the peer writes up to 3 tiles ahead)
+constexpr int kMmaLead = 2;           // score MMAs issued ahead of the value MMA
+// Value-MMA completion is tracked per tile slot T % kODone.  When tile T's scores are
+// fetched, the value MMA of tile T-3 has completed (it was issued before the score
+// MMA of T), so a slot is never more than one phase behind when it is waited on.
+constexpr int kODone = 4;
 constexpr int kThreads = 256;
 constexpr int kHeads = 128;           // MMA M (heads beyond n_heads are computed and dropped)
 constexpr int kLatHalf = 256;         // latent columns per CTA
@@ -51,22 +61,24 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStage = kOffQ + kQBytes;
 constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffBar = kOffX + 2 * kXBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers/flags + alignment slack
+constexpr uint32_t kOffBar = kOffX + kXBuf * kXBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;   // barriers/flags + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier indices
 enum : int {
     B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
-    B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY = B_PFULL + 2, B_ODONE = B_PEMPTY + 2,
-    B_OFREE, B_XFULL, B_XEMPTY = B_XFULL + 2, B_FIN = B_XEMPTY + 2, B_COUNT
+    B_SEMPTY = B_SFULL + kSBuf, B_PFULL = B_SEMPTY + kSBuf, B_PEMPTY = B_PFULL + 2,
+    B_ODONE = B_PEMPTY + 2, B_OFREE = B_ODONE + kODone, B_XFULL, B_FIN = B_XFULL + kXBuf, B_COUNT
 };
-static_assert(B_COUNT * 8 <= 200, "barrier area");
+static_assert(B_COUNT * 8 <= 448, "barrier area");
+constexpr uint32_t kOffTslot = kOffBar + 448;
+constexpr uint32_t kOffAbort = kOffBar + 452;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;          // O_r: 256 columns
-constexpr uint32_t kColS = 256;        // S: 2 x 32 columns
+constexpr uint32_t kColS = 256;        // S: kSBuf x 32 columns
 
 struct TcArgs {
     const int64_t* row_off;
@@ -121,6 +133,28 @@ struct SegWalk {
         cur = seq0 + s.hi;
         first = false;
         return true;
+    }
+};
+
+// The worker's tiles in order: global tile index T, piece index si, tile t of ntiles.
+struct TileIt {
+    SegWalk walk;
+    Seg seg;
+    int t = -1, ntiles = 0;
+    uint32_t T = 0xffffffffu, si = 0xffffffffu;
+    __device__ bool next() {
+        if (t + 1 < ntiles) { ++t; ++T; return true; }
+        if (!walk.next(seg)) return false;
+        ++si;
+        ++T;
+        t = 0;
+        ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
+        return true;
+    }
+    __device__ bool first_tile() const { return t == 0; }
+    __device__ bool last_tile() const { return t == ntiles - 1; }
+    __device__ int valid_rows() const {
+        return (int)min((int64_t)kTok, seg.hi - seg.lo - (int64_t)t * kTok);
     }
 };
 
@@ -179,8 +213,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     const uint32_t base = smem_addr(sm);
     const uint32_t sQ = base + kOffQ, sStage = base + kOffStage, sP = base + kOffP, sX = base + kOffX;
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
-    uint32_t* tslot = (uint32_t*)(sm + kOffBar + 200);
-    volatile int* abort_flag = (volatile int*)(sm + kOffBar + 204);
+    uint32_t* tslot = (uint32_t*)(sm + kOffTslot);
+    volatile int* abort_flag = (volatile int*)(sm + kOffAbort);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
@@ -191,15 +225,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
         mbar_init(bar(B_QFULL), 1);
         mbar_init(bar(B_QEMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_SFULL + i), 1);
-            mbar_init(bar(B_SEMPTY + i), 128);
-            mbar_init(bar(B_PFULL + i), 128);
-            mbar_init(bar(B_PEMPTY + i), 1);
-            mbar_init(bar(B_XFULL + i), 128);
-            mbar_init(bar(B_XEMPTY + i), 128);
-        }
-        mbar_init(bar(B_ODONE), 1);
+        for (int i = 0; i < kSBuf; ++i) { mbar_init(bar(B_SFULL + i), 1); mbar_init(bar(B_SEMPTY + i), 128); }
+        for (int i = 0; i < 2; ++i) { mbar_init(bar(B_PFULL + i), 128); mbar_init(bar(B_PEMPTY + i), 1); }
+        for (int i = 0; i < kXBuf; ++i) mbar_init(bar(B_XFULL + i), 1);
+        for (int i = 0; i < kODone; ++i) mbar_init(bar(B_ODONE + i), 1);
         mbar_init(bar(B_OFREE), 128);
         mbar_init(bar(B_FIN), 1);
         *abort_flag = 0;
@@ -214,17 +243,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         prefetch_tmap(&map_q128); prefetch_tmap(&map_q64);
     }
     tc_fence_before();
-    cluster_sync();                 // barriers of both CTAs initialised before any remote arrive
+    cluster_sync();                 // barriers of both CTAs initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem = *tslot;
-
-    SegWalk walk;
-    walk.init(a.cum, a.batch, g, S.per, S.total);
-    Seg seg;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            SegWalk walk;
+            walk.init(a.cum, a.batch, g, S.per, S.total);
+            Seg seg;
             uint32_t T = 0, si = 0;
             bool ok = true;
             while (ok && walk.next(seg)) {
@@ -235,6 +263,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 for (int j = 0; j < 4; ++j)
                     tma_load_2d(sQ + j * kQBox, &map_q128, rank * kLatHalf + 64 * j, qy, bar(B_QFULL));
                 tma_load_2d(sQ + 4 * kQBox, &map_q64, 512 + rank * kRopeHalf, qy, bar(B_QFULL));
+                ++si;
                 const int64_t row0 = a.row_off[seg.b] + seg.lo;
                 const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
                 for (int t = 0; t < ntiles; ++t, ++T) {
@@ -248,7 +277,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
                     tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
                 }
-                ++si;
             }
             // drain: every copy this thread issued has landed before the CTA may exit
             for (uint32_t k = 0; k < kStages && k < T; ++k) {
@@ -262,53 +290,55 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
             const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
-            uint32_t T = 0, si = 0;
+            TileIt sc, pv;                              // score-MMA and value-MMA positions
+            sc.walk.init(a.cum, a.batch, g, S.per, S.total);
+            pv.walk.init(a.cum, a.batch, g, S.per, S.total);
             bool ok = true;
-            bool have_prev = false;
-            uint32_t pT = 0, pSeg = 0;
-            bool pFirst = false;
-            auto issue_pv = [&](uint32_t Tp, uint32_t segp, bool firstp) -> bool {
-                const uint32_t sb = Tp & 1, st = Tp % kStages;
-                if (!wait<false>(bar(B_PFULL + sb), (Tp >> 1) & 1, ctl)) return false;
-                if (firstp && segp > 0 && !wait<false>(bar(B_OFREE), (segp - 1) & 1, ctl)) return false;
+            auto issue_score = [&]() -> bool {
+                const uint32_t T = sc.T, st = T % kStages, sb = T % kSBuf;
+                if (sc.first_tile() && !wait<false>(bar(B_QFULL), sc.si & 1, ctl)) return false;
+                if (!wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl)) return false;
+                if (!wait<false>(bar(B_SEMPTY + sb), ((T / kSBuf) & 1) ^ 1, ctl)) return false;
+                tc_fence_after();
+                const uint32_t stage = sStage + st * kStageBytes;
+                const uint32_t d = tmem + kColS + sb * kTok;
+                for (int j = 0; j < 4; ++j)
+                    for (int k = 0; k < 4; ++k)
+                        mma_bf16(d, kdesc128(sQ + j * kQBox + 32 * k), kdesc128(stage + j * kTBox + 32 * k),
+                                 id_s, (j | k) ? 1u : 0u);
+                for (int k = 0; k < 2; ++k)
+                    mma_bf16(d, kdesc64(sQ + 4 * kQBox + 32 * k), kdesc64(stage + 4 * kTBox + 32 * k), id_s, 1u);
+                mma_commit(bar(B_SFULL + sb));
+                if (sc.last_tile()) mma_commit(bar(B_QEMPTY));
+                return true;
+            };
+            auto issue_value = [&]() -> bool {
+                const uint32_t T = pv.T, st = T % kStages, pb = T & 1;
+                if (!wait<false>(bar(B_PFULL + pb), (T >> 1) & 1, ctl)) return false;
+                if (pv.first_tile() && pv.si > 0 && !wait<false>(bar(B_OFREE), (pv.si - 1) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t stage = sStage + st * kStageBytes;
                 for (int k = 0; k < kTok / 16; ++k)
-                    mma_bf16(tmem + kColO, kdesc64(sP + sb * kPBytes + 32 * k),
-                             mndesc128(stage + 2048 * k), id_o, (firstp && k == 0) ? 0u : 1u);
+                    mma_bf16(tmem + kColO, kdesc64(sP + pb * kPBytes + 32 * k), mndesc128(stage + 2048 * k),
+                             id_o, (pv.first_tile() && k == 0) ? 0u : 1u);
                 mma_commit(bar(B_EMPTY + st));
-                mma_commit(bar(B_PEMPTY + sb));
-                mma_commit(bar(B_ODONE));
+                mma_commit(bar(B_PEMPTY + pb));
+                mma_commit(bar(B_ODONE + T % kODone));
                 return true;
             };
-            while (ok && walk.next(seg)) {
-                ok = wait<false>(bar(B_QFULL), si & 1, ctl);
-                if (!ok) break;
-                const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
-                for (int t = 0; t < ntiles && ok; ++t, ++T) {
-                    const uint32_t st = T % kStages, sb = T & 1;
-                    ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl) &&
-                         wait<false>(bar(B_SEMPTY + sb), ((T >> 1) & 1) ^ 1, ctl);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t stage = sStage + st * kStageBytes;
-                    const uint32_t d = tmem + kColS + sb * kTok;
-                    for (int j = 0; j < 4; ++j)
-                        for (int k = 0; k < 4; ++k)
-                            mma_bf16(d, kdesc128(sQ + j * kQBox + 32 * k), kdesc128(stage + j * kTBox + 32 * k),
-                                     id_s, (j | k) ? 1u : 0u);
-                    for (int k = 0; k < 2; ++k)
-                        mma_bf16(d, kdesc64(sQ + 4 * kQBox + 32 * k), kdesc64(stage + 4 * kTBox + 32 * k),
-                                 id_s, 1u);
-                    mma_commit(bar(B_SFULL + sb));
-                    if (t == ntiles - 1) mma_commit(bar(B_QEMPTY));
-                    if (have_prev) ok = issue_pv(pT, pSeg, pFirst);
-                    have_prev = true;
-                    pT = T; pSeg = si; pFirst = (t == 0);
-                }
-                ++si;
+            bool more = sc.next();
+            for (int k = 0; k < kMmaLead && more && ok; ++k) {
+                ok = issue_score();
+                more = sc.next();
             }
-            if (ok && have_prev) issue_pv(pT, pSeg, pFirst);
+            while (ok && pv.next()) {
+                if (more) {
+                    ok = issue_score();
+                    more = sc.next();
+                    if (!ok) break;
+                }
+                ok = issue_value();
+            }
             mma_commit(bar(B_FIN));
             drain(bar(B_FIN), 0);
         }
@@ -318,99 +348,113 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t peer_x = mapa(sX, peer);
         const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
-        const uint32_t peer_xempty = mapa(bar(B_XEMPTY), peer);
         const uint32_t xrow = (uint32_t)i * (kTok * 4);   // this row's 128 bytes in an X buffer
-        uint32_t T = 0, si = 0;
+        TileIt fe, co;                                  // fetch/send position, consume position
+        fe.walk.init(a.cum, a.batch, g, S.per, S.total);
+        co.walk.init(a.cum, a.batch, g, S.per, S.total);
         bool ok = true;
-        while (ok && walk.next(seg)) {
-            float m_run = -INFINITY, l_run = 0.f;
-            const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
-            for (int t = 0; t < ntiles; ++t, ++T) {
-                const uint32_t sb = T & 1, par = (T >> 1) & 1, st = T % kStages;
-                float s[kTok];
-                if (!(ok = wwait<false>(bar(B_SFULL + sb), par, ctl))) break;
-                tc_fence_after();
-                tmem_ld32(tmem + lane_base + kColS + sb * kTok, s);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar(B_SEMPTY + sb));
-                // send my partial scores into the peer's X buffer, then take the peer's
-                if (!(ok = wwait<true>(bar(B_XEMPTY + sb), par ^ 1, ctl))) break;
-                for (int c = 0; c < kTok / 4; ++c) {
-                    const uint32_t off = xrow + (uint32_t)((c ^ (i & 7)) * 16);
-                    st_cluster_v4(peer_x + sb * kXBytes + off, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-                }
-                mbar_arrive_remote(peer_xfull + 8 * sb);
-                if (!(ok = wwait<true>(bar(B_XFULL + sb), par, ctl))) break;
-                const uint8_t* xb = sm + kOffX + sb * kXBytes + xrow;
-                for (int c = 0; c < kTok / 4; ++c) {
-                    const float4 v = *(const float4*)(xb + ((c ^ (i & 7)) * 16));
-                    s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
-                }
-                mbar_arrive_remote(peer_xempty + 8 * sb);
-                // rows past the end of this piece do not count
-                const int valid = (int)min((int64_t)kTok, seg.hi - seg.lo - (int64_t)t * kTok);
-                float mt = -INFINITY;
+        float s_cur[kTok], s_nxt[kTok];
+        // take this CTA's partial scores of tile fe.T out of TMEM and send them to the peer
+        auto fetch_send = [&](float (&s)[kTok]) -> bool {
+            const uint32_t T = fe.T, sb = T % kSBuf, xb = T % kXBuf;
+            if (!wwait<false>(bar(B_SFULL + sb), (T / kSBuf) & 1, ctl)) return false;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + kColS + sb * kTok, s);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(B_SEMPTY + sb));
+            if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);     // the peer's copy of tile T
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) {
-                    if (j >= valid) s[j] = -INFINITY;
-                    mt = fmaxf(mt, s[j]);
-                }
-                // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
-                const bool need = mt > m_run + 8.f;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = exp2f(m_run - mt);
-                    m_run = mt;
-                    l_run *= alpha;
-                }
-                if (t > 0 && __any_sync(0xffffffffu, need)) {
-                    if (!(ok = wwait<false>(bar(B_ODONE), (T - 1) & 1, ctl))) break;
-                    tc_fence_after();
-                    for (int c = 0; c < kLatHalf / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                        tmem_st32(tmem + lane_base + kColO + 32 * c, o);
-                    }
-                    tmem_wait_st();
-                }
-                // P tile (bf16) for the value MMA; the sum uses the rounded values
-                if (!(ok = wwait<false>(bar(B_PEMPTY + sb), par ^ 1, ctl))) break;
-                uint32_t packed[kTok / 2];
-#pragma unroll
-                for (int j = 0; j < kTok / 2; ++j) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_run), exp2f(s[2 * j + 1] - m_run));
-                    l_run += __low2float(h2) + __high2float(h2);
-                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
-                uint8_t* prow = sm + kOffP + sb * kPBytes + i * 64;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *(uint4*)(prow + ((c ^ ((i >> 1) & 3)) * 16)) =
-                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                if (valid < kTok) {
-                    // the value MMA must not see rows of the tile beyond the piece (they may
-                    // hold anything): zero them in this CTA's latent half of the stage
-                    uint8_t* stage = sm + kOffStage + st * kStageBytes;
-                    for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
-                        const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
-                        *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(bar(B_PFULL + sb));
+            for (int c = 0; c < kTok / 4; ++c) {
+                const uint32_t off = xb * kXBytes + xrow + (uint32_t)((c ^ (i & 7)) * 16);
+                st_async_v4(peer_x + off, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], peer_xfull + 8 * xb);
             }
-            if (!ok) break;
+            return true;
+        };
+        bool more = fe.next();
+        if (more) { ok = fetch_send(s_cur); more = fe.next(); }
+        float m_run = -INFINITY, l_run = 0.f;
+        while (ok && co.next()) {
+            const uint32_t T = co.T, pb = T & 1, xb = T % kXBuf, st = T % kStages;
+            if (more) {
+                if (!(ok = fetch_send(s_nxt))) break;
+                more = fe.next();
+            }
+            if (co.first_tile()) { m_run = -INFINITY; l_run = 0.f; }
+            // add the peer's partial scores of tile T
+            if (!(ok = wwait<true>(bar(B_XFULL + xb), (T / kXBuf) & 1, ctl))) break;
+            const uint8_t* xr = sm + kOffX + xb * kXBytes + xrow;
+#pragma unroll
+            for (int c = 0; c < kTok / 4; ++c) {
+                const float4 v = *(const float4*)(xr + ((c ^ (i & 7)) * 16));
+                s_cur[4 * c] += v.x; s_cur[4 * c + 1] += v.y; s_cur[4 * c + 2] += v.z; s_cur[4 * c + 3] += v.w;
+            }
+            // rows past the end of this piece do not count
+            const int valid = co.valid_rows();
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) {
+                if (j >= valid) s_cur[j] = -INFINITY;
+                mt = fmaxf(mt, s_cur[j]);
+            }
+            // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
+            const bool need = mt > m_run + 8.f;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2f(m_run - mt);
+                m_run = mt;
+                l_run *= alpha;
+            }
+            if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
+                if (!(ok = wwait<false>(bar(B_ODONE + (T - 1) % kODone), ((T - 1) / kODone) & 1, ctl))) break;
+                tc_fence_after();
+                for (int c = 0; c < kLatHalf / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= alpha;
+                    tmem_st32(tmem + lane_base + kColO + 32 * c, o);
+                }
+                tmem_wait_st();
+            }
+            // P tile (bf16) for the value MMA; the sum uses the rounded values
+            if (!(ok = wwait<false>(bar(B_PEMPTY + pb), ((T >> 1) & 1) ^ 1, ctl))) break;
+            uint32_t packed[kTok / 2];
+#pragma unroll
+            for (int j = 0; j < kTok / 2; ++j) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s_cur[2 * j] - m_run),
+                                                                exp2f(s_cur[2 * j + 1] - m_run));
+                l_run += __low2float(h2) + __high2float(h2);
+                packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            uint8_t* prow = sm + kOffP + pb * kPBytes + i * 64;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *(uint4*)(prow + ((c ^ ((i >> 1) & 3)) * 16)) =
+                    make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            if (valid < kTok) {
+                // the value MMA must not see rows of the tile beyond the piece (they may
+                // hold anything): zero them in this CTA's latent half of the stage
+                uint8_t* stage = sm + kOffStage + st * kStageBytes;
+                for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
+                    const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
+                    *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL + pb));
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) s_cur[j] = s_nxt[j];
+            if (!co.last_tile()) continue;
             // epilogue of this piece: O_r / l, log2-sum-exp
-            if (!(ok = wwait<false>(bar(B_ODONE), (T - 1) & 1, ctl))) break;
+            if (!(ok = wwait<false>(bar(B_ODONE + T % kODone), (T / kODone) & 1, ctl))) break;
             tc_fence_after();
             const float inv = 1.f / l_run;
             const float lse2 = m_run + log2f(l_run);
             const bool row_ok = i < a.n_h;
+            const Seg& seg = co.seg;
             for (int c = 0; c < kLatHalf / 32; ++c) {
                 float o[32];
                 tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
@@ -443,7 +487,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             }
             tc_fence_before();
             mbar_arrive(bar(B_OFREE));
-            ++si;
         }
     }
     // ---------------------------------------------------------------- teardown

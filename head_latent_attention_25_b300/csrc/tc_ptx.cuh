@@ -90,6 +90,15 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  "f"(c), "f"(d) : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory that counts its bytes
+// towards that CTA's mbarrier transaction count (no fence needed by the sender).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint32_t bar) {
