@@ -19,7 +19,7 @@ MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
             "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",
-            "mla_profile_events")
+            "mla_profile_events", "mla_append_workspace_size")
 
 
 class MlaDims(ctypes.Structure):
@@ -48,7 +48,9 @@ def load():
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     D = ctypes.POINTER(MlaDims)
-    lib.mla_cache_append.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P, I64, P, P]
+    lib.mla_cache_append.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P, I64, P, SZ, P, P]
+    lib.mla_append_workspace_size.argtypes = [D, I32, I32, I32]
+    lib.mla_append_workspace_size.restype = SZ
     lib.mla_cache_append.restype = I32
     lib.mla_project_query.argtypes = [D, I32, I32, I32, P, P, P, P, P, P]
     lib.mla_project_query.restype = I32
@@ -56,7 +58,7 @@ def load():
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
     lib.mla_decode_absorbed.restype = I32
-    lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P]
+    lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P, P]
     lib.mla_project_out.restype = I32
     lib.mla_status_string.argtypes = [I32]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -101,11 +103,16 @@ def make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base=10000.0, softmax_scale=0
     return MlaDims(n_heads, d_h, d_c, d_r, hidden, rope_base, softmax_scale)
 
 
+def mla_append_workspace_size(dims, dtype, batch, n_new) -> int:
+    return int(load().mla_append_workspace_size(ctypes.byref(dims), dtype, batch, n_new))
+
+
 def mla_cache_append(dims, dtype, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cache,
-                     cache_rows, dev_status, stream=None):
+                     cache_rows, workspace, workspace_bytes, dev_status, stream=None):
     _check("mla_cache_append", load().mla_cache_append(
         ctypes.byref(dims), dtype, batch, n_new, _p(h), _p(w_dkv), _p(w_kr), _p(row_off), _p(cap),
-        _p(pos0), _p(cache), cache_rows, _p(dev_status), _stream(stream)))
+        _p(pos0), _p(cache), cache_rows, _p(workspace), workspace_bytes, _p(dev_status),
+        _stream(stream)))
 
 
 def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, stream=None):
@@ -128,9 +135,10 @@ def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, r
         _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
 
 
-def mla_project_out(dims, dtype, batch, o_lat, w_uv, out, stream=None):
+def mla_project_out(dims, dtype, batch, o_lat, w_uv, out, dev_status, stream=None):
     _check("mla_project_out", load().mla_project_out(
-        ctypes.byref(dims), dtype, batch, _p(o_lat), _p(w_uv), _p(out), _stream(stream)))
+        ctypes.byref(dims), dtype, batch, _p(o_lat), _p(w_uv), _p(out), _p(dev_status),
+        _stream(stream)))
 
 
 def mla_launch_count() -> int:

@@ -139,10 +139,17 @@ mla_status mla_profile_events(void* start, void* stop) {
     return MLA_OK;
 }
 
+size_t mla_append_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new) {
+    if (!dims_ok(dims) || !dtype_ok(dtype) || batch < 1 || n_new < 1) return 0;
+    if (dtype != MLA_BF16 || !gemm_tc_shapes_ok(*dims)) return 0;
+    return append_tc_workspace(*dims, batch * n_new, nullptr, sm_count());
+}
+
 mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
                             const void* h, const void* w_dkv, const void* w_kr,
                             const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
-                            void* cache, int64_t cache_rows, int32_t* dev_status, void* stream) {
+                            void* cache, int64_t cache_rows, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30) || cache_rows < 1)
         return MLA_ERR_INVALID_ARG;
@@ -150,9 +157,17 @@ mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch
         return MLA_ERR_INVALID_ARG;
     const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == MLA_BF16 && gemm_tc_shapes_ok(*dims)) {
+        const int sms = sm_count();
+        const size_t need = append_tc_workspace(*dims, batch * n_new, nullptr, sms);
+        if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+        if (!aligned(h, 16) || !aligned(w_dkv, 16) || !aligned(w_kr, 16)) return MLA_ERR_INVALID_ARG;
+        return cuda_status(launch_append_tc(*dims, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0,
+                                            cache, cache_rows, workspace, dev_status, sms, s));
+    }
     return cuda_status(launch_append(*dims, dtype == MLA_BF16, batch, n_new, h, w_dkv, w_kr,
-                                     row_off, cap, pos0, cache, cache_rows, dev_status,
-                                     (cudaStream_t)stream));
+                                     row_off, cap, pos0, cache, cache_rows, dev_status, s));
 }
 
 mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
@@ -205,7 +220,13 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
     float* part_l = (float*)(ws + p.ws.pl_off);
     const bool bf16 = dtype == MLA_BF16;
     const float alpha = scale_of(dims) * kLog2e;
-    cudaError_t e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
+    cudaError_t e;
+    if (tc && gemm_tc_shapes_ok(*dims) && aligned(q_c, 16) && aligned(w_uk, 16)) {
+        e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s);
+        if (e == cudaSuccess) e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s);
+    } else {
+        e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
+    }
     if (e == cudaSuccess)
         e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, dev_status, s);
     if (e == cudaSuccess) {
@@ -222,11 +243,13 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
 }
 
 mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o_lat,
-                           const void* w_uv, void* out, void* stream) {
+                           const void* w_uv, void* out, int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
-    if (batch < 1 || !o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
-    return cuda_status(launch_project_out(*dims, dtype == MLA_BF16, batch, o_lat, w_uv, out,
-                                          (cudaStream_t)stream));
+    if (batch < 1 || !o_lat || !w_uv || !out || !dev_status) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (dtype == MLA_BF16 && gemm_tc_shapes_ok(*dims) && aligned(o_lat, 16) && aligned(w_uv, 16))
+        return cuda_status(launch_project_out_tc(*dims, batch, o_lat, w_uv, out, dev_status, s));
+    return cuda_status(launch_project_out(*dims, dtype == MLA_BF16, batch, o_lat, w_uv, out, s));
 }
 
 }  // extern "C"

@@ -1,0 +1,404 @@
+// Weight-stationary tcgen05 GEMM for the projections around the attention core.
+//
+//   D[m, t] = sum_k W_g[m, k] X_g[t, k]      m: output feature, t: token, g: head
+//
+// The weights are the A operand (M = 128 output features per tile, TMA-loaded, K-major
+// or MN-major), the tokens are the B operand (N <= 128 per tile), the accumulator
+// lives in TMEM, and K is cut into 64-wide chunks streamed through a 4-stage ring.
+// For the cache append the long K (hidden = 7168) is also split across CTAs, which
+// write fp32 partial sums; a finalize kernel adds them in a fixed order, rotates the
+// k_R pairs and stores the bf16 cache rows.
+#include <mutex>
+
+#include "mla_common.cuh"
+#include "mla_internal.h"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kGM = 128;              // output features per tile (MMA M)
+constexpr int kGK = 64;               // K chunk (one 128-byte swizzle row of bf16)
+constexpr int kGNMax = 128;           // tokens per tile (MMA N)
+constexpr int kGStages = 4;
+constexpr int kGThreads = 128;
+constexpr uint32_t kATile = kGM * kGK * 2;      // 16 KB
+constexpr uint64_t kGTimeoutNs = 2000000000ull;
+
+// Shared memory per token-tile width: kGStages x (A tile + B tile) + barriers.
+template <int NT>
+struct GemmSmem {
+    static constexpr uint32_t kBTile = NT * kGK * 2;
+    static constexpr uint32_t kStage = kATile + kBTile;
+    static constexpr uint32_t kOffBar = kGStages * kStage;
+    static constexpr uint32_t kBytes = kOffBar + 128 + 1024;
+};
+
+enum GemmMode : int { kOutBf16 = 0, kOutPartial = 1 };
+
+struct GemmTcArgs {
+    int M;                // output features (all tiles)
+    int N;                // tokens
+    int k_chunks;         // ceil(K / 64)
+    int chunks_per_split; // K chunks per CTA
+    int k_splits;
+    int a_mn;             // weights stored with the output feature contiguous (MN-major A)
+    int m_split_tile;     // M tiles >= this read the second weight map (rows - tile offset)
+    int a2_rows;          // rows loaded from the second weight map (<= 128)
+    int mode;
+    float alpha;
+    void* y; int64_t y_g, y_tok;      // bf16 output: y[g*y_g + t*y_tok + m]
+    float* part; int part_ld;         // fp32 partial: part[(split*N + t)*part_ld + m]
+    int32_t* dev_status;
+};
+
+__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* st) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kGTimeoutNs) {
+            *abort = 1;
+            if (st) atomicOr(st, MLA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void gdrain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kGTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kGThreads)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_a2,
+               const __grid_constant__ CUtensorMap map_b, GemmTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const uint32_t base = smem_addr(sm);
+    using L = GemmSmem<NT>;
+    uint64_t* bars = (uint64_t*)(sm + L::kOffBar);
+    uint32_t* tslot = (uint32_t*)(sm + L::kOffBar + 96);
+    volatile int* abort_flag = (volatile int*)(sm + L::kOffBar + 100);
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };   // 0..3 full, 4..7 empty, 8 done
+    constexpr uint32_t kBTile = L::kBTile;
+    constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m_tile = blockIdx.x, n_tile = blockIdx.y;
+    const int g = blockIdx.z / a.k_splits, ks = blockIdx.z % a.k_splits;
+    const int kc0 = ks * a.chunks_per_split;
+    const int kc1 = min(kc0 + a.chunks_per_split, a.k_chunks);
+    const bool second = m_tile >= a.m_split_tile;
+    const uint32_t a_bytes = second ? (uint32_t)a.a2_rows * kGK * 2 : kATile;
+
+    if (tid == 0) {
+        for (int i = 0; i < kGStages; ++i) { mbar_init(bar(i), 1); mbar_init(bar(4 + i), 1); }
+        mbar_init(bar(8), 1);
+        *abort_flag = 0;
+        fence_mbar_init_cluster();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_addr(tslot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0 && lane == 0) {
+        // producer
+        uint32_t i = 0;
+        for (int kc = kc0; kc < kc1; ++kc, ++i) {
+            const uint32_t st = i % kGStages;
+            if (!gwait(bar(4 + st), ((i / kGStages) & 1) ^ 1, abort_flag, a.dev_status)) break;
+            const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
+            mbar_expect_tx(bar(st), a_bytes + kBTile);
+            if (second) {
+                tma_load_3d(sa, &map_a2, kc * kGK, (m_tile - a.m_split_tile) * kGM, g, bar(st));
+            } else if (a.a_mn) {
+                tma_load_3d(sa, &map_a, m_tile * kGM, kc * kGK, g, bar(st));
+                tma_load_3d(sa + kATile / 2, &map_a, m_tile * kGM + 64, kc * kGK, g, bar(st));
+            } else {
+                tma_load_3d(sa, &map_a, kc * kGK, m_tile * kGM, g, bar(st));
+            }
+            tma_load_3d(sb, &map_b, kc * kGK, g, n_tile * NT, bar(st));
+        }
+        for (uint32_t k = 0; k < kGStages && k < i; ++k) {
+            const uint32_t j = i - 1 - k;
+            gdrain(bar(j % kGStages), (j / kGStages) & 1);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        const uint32_t idesc = idesc_bf16_f32(kGM, NT, a.a_mn && !second ? 1u : 0u, 0u);
+        uint32_t i = 0;
+        for (int kc = kc0; kc < kc1; ++kc, ++i) {
+            const uint32_t st = i % kGStages;
+            if (!gwait(bar(st), (i / kGStages) & 1, abort_flag, a.dev_status)) break;
+            tc_fence_after();
+            const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
+            for (int k = 0; k < kGK / 16; ++k) {
+                const uint64_t da = (a.a_mn && !second)
+                    ? smem_desc(sa + 2048 * k, kATile / 2, 1024, kSwizzle128B)   // MN-major: 64-wide atoms 8 KB apart
+                    : smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B);
+                mma_bf16(tmem, da, smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B), idesc,
+                         (i > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(bar(4 + st));
+        }
+        mma_commit(bar(8));
+    }
+    // epilogue: thread <-> output feature (TMEM lane), 32 tokens per TMEM load
+    __syncwarp();
+    const bool ok = gwait(bar(8), 0, abort_flag, a.dev_status);
+    tc_fence_after();
+    const int m = m_tile * kGM + warp * 32 + lane;
+    const bool m_ok = m < a.M;
+    if (__all_sync(0xffffffffu, ok)) {
+        constexpr int kChunks = NT < 32 ? 1 : NT / 32;
+        constexpr int kCols = NT < 32 ? NT : 32;
+        for (int c = 0; c < kChunks; ++c) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
+            tmem_wait_ld();
+            if (!m_ok) continue;
+            for (int j = 0; j < kCols; ++j) {
+                const int t = n_tile * NT + 32 * c + j;
+                if (t >= a.N) break;
+                if (a.mode == kOutBf16)
+                    ((__nv_bfloat16*)a.y)[(int64_t)g * a.y_g + (int64_t)t * a.y_tok + m] =
+                        __float2bfloat16_rn(a.alpha * v[j]);
+                else
+                    a.part[((int64_t)ks * a.N + t) * a.part_ld + m] = v[j];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// cache row = [sum of partials for c ; RoPE(sum of partials for k_R, pos)] in bf16
+__global__ void append_finalize_kernel(const float* part, int k_splits, int n_tok, int n_new,
+                                       int d_c, int d_r, float rope_base, const int64_t* row_off,
+                                       const int32_t* cap, const int32_t* pos0, int64_t cache_rows,
+                                       __nv_bfloat16* cache, int32_t* dev_status) {
+    const int t = blockIdx.x;
+    if (t >= n_tok) return;
+    const int b = t / n_new, j = t % n_new;
+    const int p0 = pos0[b];
+    const int64_t off = row_off[b], cp = cap[b];
+    if (p0 < 0 || (int64_t)p0 + n_new > cp || off < 0 || off + cp > cache_rows) {
+        if (j == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
+        return;
+    }
+    const int64_t pos = (int64_t)p0 + j;
+    const int width = d_c + d_r;
+    __nv_bfloat16* row = cache + (off + pos) * width;
+    for (int e = 2 * threadIdx.x; e < width; e += 2 * blockDim.x) {
+        float v0 = 0.f, v1 = 0.f;
+        for (int s = 0; s < k_splits; ++s) {
+            const float* p = part + ((int64_t)s * n_tok + t) * width + e;
+            v0 += p[0];
+            v1 += p[1];
+        }
+        if (e >= d_c) {
+            float c, sn;
+            rope_cos_sin(pos, (e - d_c) >> 1, d_r, rope_base, &c, &sn);
+            const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
+            v0 = r0; v1 = r1;
+        }
+        *(__nv_bfloat162*)(row + e) = __floats2bfloat162_rn(v0, v1);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_enc_once;
+
+bool encoder() {
+    std::call_once(g_enc_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    });
+    return g_enc != nullptr;
+}
+
+// 3-D bf16 map: dims (inner..outer) d0, d1, d2 with byte strides s1, s2; box b0 x b1 x b2.
+bool map3(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+          uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int pick_nt(int n) {
+    if (n <= 16) return 16;
+    if (n <= 32) return 32;
+    if (n <= 64) return 64;
+    return 128;
+}
+
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtensorMap& mb, GemmTcArgs a,
+                     int G, int nt, cudaStream_t s) {
+    const int m_tiles = (a.M + kGM - 1) / kGM;
+    const int n_tiles = (a.N + nt - 1) / nt;
+    dim3 grid(m_tiles, n_tiles, G * a.k_splits);
+    cudaError_t e;
+#define MLA_GEMM_CASE(NTV)                                                                         \
+    case NTV:                                                                                      \
+        e = cudaFuncSetAttribute(gemm_tc_kernel<NTV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)GemmSmem<NTV>::kBytes);                                      \
+        if (e != cudaSuccess) return e;                                                           \
+        gemm_tc_kernel<NTV><<<grid, kGThreads, GemmSmem<NTV>::kBytes, s>>>(ma, ma2, mb, a);        \
+        break;
+    switch (nt) {
+        MLA_GEMM_CASE(16)
+        MLA_GEMM_CASE(32)
+        MLA_GEMM_CASE(64)
+        MLA_GEMM_CASE(128)
+        default: return cudaErrorInvalidValue;
+    }
+#undef MLA_GEMM_CASE
+    note_launch();
+    return cudaGetLastError();
+}
+
+GemmTcArgs gblank() {
+    GemmTcArgs a{};
+    a.k_splits = 1;
+    a.m_split_tile = 1 << 30;
+    a.alpha = 1.f;
+    a.mode = kOutBf16;
+    return a;
+}
+
+}  // namespace
+
+bool gemm_tc_shapes_ok(const mla_dims& d) {
+    return d.d_c % 128 == 0 && d.d_h % 128 == 0 && d.d_r % 16 == 0 && d.d_r <= 128 &&
+           d.hidden % 64 == 0;
+}
+
+size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count) {
+    const int k_chunks = (d.hidden + kGK - 1) / kGK;
+    const int m_tiles = (d.d_c + d.d_r + kGM - 1) / kGM;
+    const int n_tiles = (n_tok + kGNMax - 1) / kGNMax;
+    int want = (sm_count > 0 ? sm_count : 148) / (m_tiles * n_tiles);
+    if (want < 1) want = 1;
+    int per = (k_chunks + want - 1) / want;
+    if (per < 2) per = 2;
+    const int splits = (k_chunks + per - 1) / per;
+    if (k_splits_out) *k_splits_out = splits;
+    return align_up((size_t)splits * n_tok * (d.d_c + d.d_r) * sizeof(float), 256);
+}
+
+cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
+                             const void* w_kr, const int64_t* row_off, const int32_t* cap,
+                             const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                             int32_t* dev_status, int sm_count, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const int n_tok = batch * n_new;
+    int splits = 1;
+    append_tc_workspace(d, n_tok, &splits, sm_count);
+    const int width = d.d_c + d.d_r;
+    const int k_chunks = (d.hidden + kGK - 1) / kGK;
+    const int nt = pick_nt(n_tok);
+    CUtensorMap ma, ma2, mb;
+    const uint64_t H = d.hidden;
+    if (!map3(&ma, w_dkv, H, d.d_c, 1, H * 2, H * 2 * d.d_c, kGK, kGM, 1) ||
+        !map3(&ma2, w_kr, H, d.d_r, 1, H * 2, H * 2 * d.d_r, kGK, d.d_r, 1) ||
+        !map3(&mb, h, H, 1, n_tok, H * 2, H * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = width;
+    a.N = n_tok;
+    a.k_chunks = k_chunks;
+    a.k_splits = splits;
+    a.chunks_per_split = (k_chunks + splits - 1) / splits;
+    a.m_split_tile = d.d_c / kGM;
+    a.a2_rows = d.d_r;
+    a.mode = kOutPartial;
+    a.part = (float*)workspace;
+    a.part_ld = width;
+    a.dev_status = dev_status;
+    cudaError_t e = run_gemm(ma, ma2, mb, a, 1, nt, s);
+    if (e != cudaSuccess) return e;
+    append_finalize_kernel<<<n_tok, 128, 0, s>>>((const float*)workspace, splits, n_tok, n_new, d.d_c,
+                                                 d.d_r, d.rope_base, row_off, cap, pos0, cache_rows,
+                                                 (__nv_bfloat16*)cache, dev_status);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const void* w_uk, float alpha,
+                           void* qp, int32_t* dev_status, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const int nt = pick_nt(batch);
+    const uint64_t dc = d.d_c, dh = d.d_h, nh = d.n_heads;
+    CUtensorMap ma, mb;
+    // W_UK [n_h, d_h, d_c]: the output feature c is contiguous (MN-major A), K = d_h
+    if (!map3(&ma, w_uk, dc, dh, nh, dc * 2, dc * dh * 2, 64, kGK, 1) ||
+        !map3(&mb, q_c, dh, nh, batch, dh * 2, dh * nh * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = d.d_c;
+    a.N = batch;
+    a.k_chunks = (d.d_h + kGK - 1) / kGK;
+    a.chunks_per_split = a.k_chunks;
+    a.a_mn = 1;
+    a.alpha = alpha;
+    a.y = qp;
+    a.y_g = d.d_c + d.d_r;
+    a.y_tok = (int64_t)d.n_heads * (d.d_c + d.d_r);
+    a.dev_status = dev_status;
+    return run_gemm(ma, ma, mb, a, d.n_heads, nt, s);
+}
+
+cudaError_t launch_project_out_tc(const mla_dims& d, int batch, const void* o_lat, const void* w_uv,
+                                  void* out, int32_t* dev_status, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const int nt = pick_nt(batch);
+    const uint64_t dc = d.d_c, dh = d.d_h, nh = d.n_heads;
+    CUtensorMap ma, mb;
+    // W_UV [n_h, d_h, d_c]: rows are output features d, K = d_c contiguous (K-major A)
+    if (!map3(&ma, w_uv, dc, dh, nh, dc * 2, dc * dh * 2, kGK, kGM, 1) ||
+        !map3(&mb, o_lat, dc, nh, batch, dc * 2, dc * nh * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = d.d_h;
+    a.N = batch;
+    a.k_chunks = (d.d_c + kGK - 1) / kGK;
+    a.chunks_per_split = a.k_chunks;
+    a.y = out;
+    a.y_g = d.d_h;
+    a.y_tok = (int64_t)d.n_heads * d.d_h;
+    a.dev_status = dev_status;
+    return run_gemm(ma, ma, mb, a, d.n_heads, nt, s);
+}
+
+}  // namespace mla

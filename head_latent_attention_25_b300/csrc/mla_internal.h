@@ -27,6 +27,22 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
 cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const void* o_lat,
                                const void* w_uv, void* out, cudaStream_t s);
 
+// The rotary part of Q' alone (the content part comes from a GEMM).
+cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
+                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s);
+
+// tcgen05 projections (bf16; shapes accepted by gemm_tc_shapes_ok)
+bool gemm_tc_shapes_ok(const mla_dims& d);
+size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count);
+cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
+                             const void* w_kr, const int64_t* row_off, const int32_t* cap,
+                             const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                             int32_t* dev_status, int sm_count, cudaStream_t s);
+cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const void* w_uk, float alpha,
+                           void* qp, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_project_out_tc(const mla_dims& d, int batch, const void* o_lat, const void* w_uv,
+                                  void* out, int32_t* dev_status, cudaStream_t s);
+
 // Work split of the flattened context: prefix sums of the usable sequence lengths and
 // the Schedule, written into the workspace; flags unusable sequences.
 cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,

@@ -134,21 +134,26 @@ GemmArgs blank() {
 }
 
 // Q'[b, i, d_c + 2k .. 2k+1] = alpha * RoPE(q_R[b, i, :], seq_len[b] - 1) pair k.
+// One block per sequence: the d_r/2 angles are shared by all heads.
+constexpr int kMaxRopePairs = 512;
+
 template <typename Tin, typename Tout>
 __global__ void fold_rope_kernel(const Tin* q_r, const int32_t* seq_len, Tout* qp, int n_h, int d_c,
                                  int d_r, float base, float alpha, int batch) {
-    const int bi = blockIdx.x;           // b * n_h + i
-    const int b = bi / n_h;
+    __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
+    const int b = blockIdx.x;
     if (b >= batch) return;
+    const int half = d_r / 2;
     const int64_t pos = seq_len[b] > 0 ? (int64_t)seq_len[b] - 1 : 0;
-    const Tin* src = q_r + (int64_t)bi * d_r;
-    Tout* dst = qp + (int64_t)bi * (d_c + d_r) + d_c;
-    for (int k = threadIdx.x; k < d_r / 2; k += blockDim.x) {
-        float c, s;
-        rope_cos_sin(pos, k, d_r, base, &c, &s);
-        float x0 = ld(src + 2 * k), x1 = ld(src + 2 * k + 1);
-        st(dst + 2 * k, alpha * (x0 * c - x1 * s));
-        st(dst + 2 * k + 1, alpha * (x0 * s + x1 * c));
+    for (int k = threadIdx.x; k < half; k += blockDim.x) rope_cos_sin(pos, k, d_r, base, &cs[k], &sn[k]);
+    __syncthreads();
+    for (int e = threadIdx.x; e < n_h * half; e += blockDim.x) {
+        const int i = e / half, k = e - i * half;
+        const Tin* src = q_r + ((int64_t)b * n_h + i) * d_r;
+        Tout* dst = qp + ((int64_t)b * n_h + i) * (d_c + d_r) + d_c;
+        const float x0 = ld(src + 2 * k), x1 = ld(src + 2 * k + 1);
+        st(dst + 2 * k, alpha * (x0 * cs[k] - x1 * sn[k]));
+        st(dst + 2 * k + 1, alpha * (x0 * sn[k] + x1 * cs[k]));
     }
 }
 
@@ -196,8 +201,12 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
     a.alpha = alpha;
     cudaError_t e = dispatch(a, in_bf16, out_bf16, s);
     if (e != cudaSuccess) return e;
-    const int blocks = batch * d.n_heads;
-    const int threads = d.d_r / 2 < 32 ? 32 : (d.d_r / 2 > 256 ? 256 : d.d_r / 2);
+    return launch_fold_rope(d, in_bf16, out_bf16, batch, q_r, seq_len, alpha, qp, s);
+}
+
+cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
+                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s) {
+    const int blocks = batch, threads = 256;
     if (in_bf16) {
         if (out_bf16)
             fold_rope_kernel<<<blocks, threads, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,

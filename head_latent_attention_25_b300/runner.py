@@ -62,6 +62,8 @@ class DecodeStep:
         if self.ws_bytes == 0:
             raise L.MlaError("mla_decode_workspace_size", L.MLA_ERR_UNSUPPORTED)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.app_ws_bytes = L.mla_append_workspace_size(self.dims, self.dt, B, n_new)
+        self.app_workspace = torch.empty(max(self.app_ws_bytes, 256), dtype=torch.uint8, device=device)
         self.w = {}
 
     # ------------------------------------------------------------------ inputs
@@ -87,7 +89,8 @@ class DecodeStep:
     def append(self, stream=None):
         L.mla_cache_append(self.dims, self.dt, self.batch, self.n_new, self.h, self.w["w_dkv"],
                            self.w["w_kr"], self.row_off, self.cap, self.pos0, self.cache,
-                           self.total_rows, self.dev_status, stream)
+                           self.total_rows, self.app_workspace, self.app_ws_bytes, self.dev_status,
+                           stream)
 
     def project_query(self, stream=None):
         L.mla_project_query(self.dims, self.dt, self.batch, self.d_q_in, self.x_q, self.w["w_uq"],
@@ -106,7 +109,8 @@ class DecodeStep:
                               self.lse if lse is None else lse, self.dev_status, stream)
 
     def project_out(self, stream=None):
-        L.mla_project_out(self.dims, self.dt, self.batch, self.o_lat, self.w["w_uv"], self.out, stream)
+        L.mla_project_out(self.dims, self.dt, self.batch, self.o_lat, self.w["w_uv"], self.out,
+                          self.dev_status, stream)
 
     def step(self, stream=None):
         """The whole path: append, [query projection], decode, up-projection."""

@@ -97,6 +97,8 @@ typedef struct {
  *   cache    rows of d_c + d_r        token t of sequence b goes to row
  *                                     row_off[b] + pos0[b] + t, rotated at position pos0[b] + t
  *   cache_rows                        rows in the cache buffer (host value, >= 1)
+ *   workspace  device scratch of at least mla_append_workspace_size(dims, dtype, batch, n_new)
+ *              bytes, 256-byte aligned (may be NULL when that size is 0); contents ignored
  *   dev_status int32 (device)         MLA_DEV_BAD_POSITION is OR-ed in for a sequence whose
  *                                     new rows would leave [0, cap[b]) or the buffer
  *                                     (row_off[b] < 0 or row_off[b] + cap[b] > cache_rows);
@@ -106,7 +108,16 @@ typedef struct {
 MLA_API mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
                             const void* h, const void* w_dkv, const void* w_kr,
                             const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
-                            void* cache, int64_t cache_rows, int32_t* dev_status, void* stream);
+                            void* cache, int64_t cache_rows, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * mla_append_workspace_size -- bytes of device workspace mla_cache_append needs (bf16
+ * with tensor-core shapes splits the long hidden reduction across CTAs and keeps
+ * fp32 partial sums there); 0 when no workspace is needed or the arguments are bad.
+ */
+MLA_API size_t mla_append_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                         int32_t n_new);
 
 /*
  * mla_project_query -- per-head query parts from a query input x (the query latent
@@ -171,9 +182,11 @@ MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, in
  * latent attention", section "The absorption trick", value side).
  *
  *   o_lat [batch, n_h, d_c]    w_uv [n_h, d_h, d_c]    out [batch, n_h, d_h]
+ *   dev_status                 MLA_DEV_TIMEOUT if a bounded wait expired
  */
 MLA_API mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_t batch,
-                           const void* o_lat, const void* w_uv, void* out, void* stream);
+                           const void* o_lat, const void* w_uv, void* out, int32_t* dev_status,
+                           void* stream);
 
 /* Static description of a status code (never NULL). */
 MLA_API const char* mla_status_string(mla_status status);

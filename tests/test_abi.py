@@ -47,9 +47,9 @@ def test_bad_dims_rejected_on_host(bad):
     d = _dims(**bad)
     lib = mla.load()
     fake = 256  # never dereferenced: the checks fail first
-    st = lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, fake, None)
+    st = lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake, None)
     assert st == mla.MLA_ERR_INVALID_ARG
-    st = lib.mla_project_out(ctypes.byref(d), 0, 1, fake, fake, fake, None)
+    st = lib.mla_project_out(ctypes.byref(d), 0, 1, fake, fake, fake, fake, None)
     assert st == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_workspace_size(ctypes.byref(d), 0, 1, 16, 4) == 0
 
@@ -58,7 +58,7 @@ def test_null_pointers_rejected_on_host():
     d = _dims()
     lib = mla.load()
     fake = 256
-    assert lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, None, fake, fake, fake, fake, fake, fake, 64, fake,
+    assert lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, None, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_absorbed(ctypes.byref(d), 0, 1, fake, fake, fake, None, 64, fake, fake, 8, 1, fake,
                                    1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
@@ -66,7 +66,7 @@ def test_null_pointers_rejected_on_host():
                                    1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_project_query(ctypes.byref(d), 0, 1, 64, fake, fake, None, fake, fake,
                                  None) == mla.MLA_ERR_INVALID_ARG
-    assert lib.mla_cache_append(None, 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, fake,
+    assert lib.mla_cache_append(None, 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
 
 
@@ -74,13 +74,13 @@ def test_misaligned_cache_and_bad_dtype_rejected():
     d = _dims()
     lib = mla.load()
     fake = 256
-    assert lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, fake, fake, fake, fake, fake, fake, fake + 4, 64, fake,
+    assert lib.mla_cache_append(ctypes.byref(d), 0, 1, 1, fake, fake, fake, fake, fake, fake, fake + 4, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
-    assert lib.mla_cache_append(ctypes.byref(d), 7, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, fake,
+    assert lib.mla_cache_append(ctypes.byref(d), 7, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
     # bf16 rows of 3 + 3 elements are 12 bytes: not a multiple of 16
     d2 = _dims(d_c=4, d_r=2)
-    assert lib.mla_cache_append(ctypes.byref(d2), 1, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, fake,
+    assert lib.mla_cache_append(ctypes.byref(d2), 1, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
 
 
