@@ -19,7 +19,7 @@ MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
             "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",
-            "mla_profile_events", "mla_append_workspace_size")
+            "mla_profile_events", "mla_append_workspace_size", "mla_decode_absorbed_noalloc")
 
 
 class MlaDims(ctypes.Structure):
@@ -59,6 +59,8 @@ def load():
     lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
     lib.mla_decode_absorbed.restype = I32
     lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P, P]
+    lib.mla_decode_absorbed_noalloc.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, P, P, P]
+    lib.mla_decode_absorbed_noalloc.restype = I32
     lib.mla_project_out.restype = I32
     lib.mla_status_string.argtypes = [I32]
     lib.mla_status_string.restype = ctypes.c_char_p
@@ -133,6 +135,15 @@ def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, r
         ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
         _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
         _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
+
+
+def mla_decode_absorbed_noalloc(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                                seq_len, max_seq_len, num_splits, o_lat, lse, dev_status, stream=None):
+    """mla_decode_absorbed without a workspace: uses the library's built-in 32 MiB scratch."""
+    _check("mla_decode_absorbed_noalloc", load().mla_decode_absorbed_noalloc(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(o_lat), _p(lse), _p(dev_status),
+        _stream(stream)))
 
 
 def mla_project_out(dims, dtype, batch, o_lat, w_uv, out, dev_status, stream=None):

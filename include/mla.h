@@ -188,6 +188,33 @@ MLA_API mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_
                            const void* o_lat, const void* w_uv, void* out, int32_t* dev_status,
                            void* stream);
 
+/*
+ * mla_decode_absorbed_noalloc -- mla_decode_absorbed for callers that cannot allocate
+ * device memory (code running where cudaMalloc is unavailable or not allowed, such as
+ * inside an allocator's own callbacks or in hosts that hand out all device memory).
+ * This entry point is an addition of this library; the pages describe no counterpart.
+ *
+ * Same arguments and results as mla_decode_absorbed, minus the workspace: the scratch
+ * is a fixed 32 MiB array compiled into the library, which every GPU that loads the
+ * library keeps until the process exits.  Nothing is allocated or freed by the call.
+ * - Returns MLA_ERR_WORKSPACE, before any CUDA call, when
+ *   mla_decode_workspace_size(dims, dtype, batch, max_seq_len, num_splits) exceeds
+ *   32 MiB (lower num_splits, batch or max_seq_len, or use mla_decode_absorbed).
+ * - The first call on a device looks up that device's address of the array
+ *   (cudaGetSymbolAddress, with the device current); make that first call before any
+ *   stream capture.
+ * - All calls on a device share the one array and it keeps the last call's contents
+ *   (nothing in it needs clearing: the decode overwrites whatever it reads).  Calls
+ *   whose work overlaps on the GPU (different streams, or host threads without
+ *   ordering) race on it and must be serialised by the caller.
+ */
+MLA_API mla_status mla_decode_absorbed_noalloc(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                       const void* q_c, const void* q_r, const void* w_uk,
+                                       const void* cache, int64_t cache_rows, const int64_t* row_off,
+                                       const int32_t* seq_len, int32_t max_seq_len,
+                                       int32_t num_splits, void* o_lat, float* lse,
+                                       int32_t* dev_status, void* stream);
+
 /* Static description of a status code (never NULL). */
 MLA_API const char* mla_status_string(mla_status status);
 
