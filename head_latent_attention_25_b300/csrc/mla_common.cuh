@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/mla.h"
@@ -20,15 +21,39 @@ __device__ __forceinline__ void st(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // ---- rotary angle -----------------------------------------------------------------
-// cos/sin of pos * theta_k, theta_k = base^(-2k/d_r).  The product is formed and
-// reduced into [-pi, pi] in fp64 so that positions up to 2^31 keep full fp32
-// accuracy after the final single-precision sincos.
-__device__ __forceinline__ void rope_cos_sin(int64_t pos, int k, int d_r, float base,
-                                             float* c, float* s) {
-    double theta = pow((double)base, -2.0 * (double)k / (double)d_r);
-    double ang = (double)pos * theta;
-    double red = ang - kTwoPi * rint(ang / kTwoPi);
+// theta_k = base^(-2k/d_r) = r^k with r = base^(-2/d_r).  The host forms r once per
+// call in fp64 (rope_ratio); the kernels raise it to the integer power k by binary
+// powering (at most 2*log2(k) fp64 products, relative error below 1e-14), form
+// pos * theta_k and reduce it into [-pi, pi] in fp64, so positions up to 2^31 keep
+// full fp32 accuracy after the final single-precision sincos.  No fp64
+// transcendental runs on the device (fp64 throughput on this part is low).
+inline double rope_ratio(float base, int d_r) { return pow((double)base, -2.0 / (double)d_r); }
+
+__device__ __forceinline__ double rope_theta(double r, int k) {
+    double t = 1.0, p = r;
+    for (; k; k >>= 1) {
+        if (k & 1) t *= p;
+        p *= p;
+    }
+    return t;
+}
+
+__device__ __forceinline__ void rope_cos_sin(int64_t pos, int k, double r, float* c, float* s) {
+    const double ang = (double)pos * rope_theta(r, k);
+    const double red = fma(-kTwoPi, rint(ang * (1.0 / kTwoPi)), ang);
     sincosf((float)red, s, c);
+}
+
+// ---- paired element access (rotary pairs, vectorised epilogues) --------------------
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld2(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st2(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void st2(__nv_bfloat16* p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -182,41 +182,91 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
 }
 
 // ------------------------------------------------------------------ merge
+// Grid (batch, head pairs): each half of the block (128 threads) merges one head of a
+// sequence that was cut across workers.  Pass 1 finds the maximum and the sum of the
+// pieces' log2-sum-exps (lanes stride over the pieces); pass 2 forms the normalised
+// piece weights in shared memory, 256 pieces at a time, and every thread adds its
+// two columns of all pieces with independent paired loads.
+constexpr int kMergeChunk = 256;
+
+__device__ __forceinline__ int64_t piece_slot(int64_t w, int64_t seq_begin, int64_t per) {
+    // the worker's first segment (slot 2w) unless the sequence starts inside its range
+    return 2 * w + (seq_begin <= w * per ? 0 : 1);
+}
+
 template <typename Tout>
-__global__ void __launch_bounds__(128) merge_kernel(const int64_t* cum, const Schedule* sched,
-                                                    const float* part_o, const float* part_l,
-                                                    Tout* o_lat, float* lse, int n_h, int d_c) {
-    const int bh = blockIdx.x;
-    const int b = bh / n_h, h = bh - b * n_h;
-    Tout* out = o_lat + (int64_t)bh * d_c;
-    if (cum[b + 1] == cum[b]) {                 // empty or rejected by the schedule
-        for (int c = threadIdx.x; c < d_c; c += blockDim.x) st(out + c, 0.f);
-        if (threadIdx.x == 0 && lse) lse[bh] = -INFINITY;
+__global__ void __launch_bounds__(256) merge_kernel(const int64_t* __restrict__ cum,
+                                                    const Schedule* __restrict__ sched,
+                                                    const float* __restrict__ part_o,
+                                                    const float* __restrict__ part_l,
+                                                    Tout* __restrict__ o_lat, float* __restrict__ lse,
+                                                    int n_h, int d_c) {
+    __shared__ float wts[2][kMergeChunk];
+    __shared__ float stat[2][2];
+    const int b = blockIdx.x;
+    const int half = threadIdx.x >> 7, t = threadIdx.x & 127;
+    const int lane = t & 31, warp_in_half = t >> 5;
+    const int h = blockIdx.y * 2 + half;
+    const bool active = h < n_h;
+    const int64_t seq0 = cum[b], seq1 = cum[b + 1];
+    Tout* out = o_lat + ((int64_t)b * n_h + (active ? h : 0)) * d_c;
+    if (seq1 == seq0) {                         // empty or rejected by the schedule
+        if (active) {
+            for (int c = 2 * t; c < d_c; c += 256) st2(out + c, 0.f, 0.f);
+            if (t == 0 && lse) lse[(int64_t)b * n_h + h] = -INFINITY;
+        }
         return;
     }
     const int64_t per = sched->per;
-    const int64_t first_w = cum[b] / per, last_w = (cum[b + 1] - 1) / per;
+    const int64_t first_w = seq0 / per, last_w = (seq1 - 1) / per;
     if (first_w == last_w) return;              // finished in place by its only worker
-    float mx = -INFINITY;
-    for (int64_t w = first_w; w <= last_w; ++w) {
-        const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
-        mx = fmaxf(mx, part_l[slot * n_h + h]);
+    const int64_t np = last_w - first_w + 1;
+    if (active && warp_in_half == 0) {
+        float mx = -INFINITY;
+        for (int64_t p = lane; p < np; p += 32)
+            mx = fmaxf(mx, part_l[piece_slot(first_w + p, seq0, per) * n_h + h]);
+        mx = warp_max(mx);
+        float L = 0.f;
+        for (int64_t p = lane; p < np; p += 32)
+            L += exp2f(part_l[piece_slot(first_w + p, seq0, per) * n_h + h] - mx);
+        L = warp_sum(L);
+        if (lane == 0) { stat[half][0] = mx; stat[half][1] = 1.f / L; }
+        if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
     }
-    float L = 0.f;
-    for (int64_t w = first_w; w <= last_w; ++w) {
-        const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
-        L += exp2f(part_l[slot * n_h + h] - mx);
-    }
-    const float inv = 1.f / L;
-    for (int c = threadIdx.x; c < d_c; c += blockDim.x) {
-        float v = 0.f;
-        for (int64_t w = first_w; w <= last_w; ++w) {
-            const int64_t slot = 2 * w + (cum[b] <= w * per ? 0 : 1);
-            v = fmaf(exp2f(part_l[slot * n_h + h] - mx), part_o[(slot * n_h + h) * d_c + c], v);
+    __syncthreads();
+    const float mx = stat[half][0], inv = stat[half][1];
+    // each thread owns columns 2t + 256k
+    constexpr int kMaxCols = 4;                 // d_c <= 1024 columns per head
+    float acc[kMaxCols][2] = {};
+    for (int64_t p0 = 0; p0 < np; p0 += kMergeChunk) {
+        const int nc = (int)min((int64_t)kMergeChunk, np - p0);
+        __syncthreads();
+        if (active)
+            for (int p = t; p < nc; p += 128)
+                wts[half][p] = exp2f(part_l[piece_slot(first_w + p0 + p, seq0, per) * n_h + h] - mx) * inv;
+        __syncthreads();
+        if (!active) continue;
+#pragma unroll 4
+        for (int p = 0; p < nc; ++p) {
+            const float wp = wts[half][p];
+            const float* src = part_o + (piece_slot(first_w + p0 + p, seq0, per) * n_h + h) * d_c;
+#pragma unroll
+            for (int k = 0; k < kMaxCols; ++k) {
+                const int c = 2 * t + 256 * k;
+                if (c < d_c) {
+                    const float2 v = *reinterpret_cast<const float2*>(src + c);
+                    acc[k][0] = fmaf(wp, v.x, acc[k][0]);
+                    acc[k][1] = fmaf(wp, v.y, acc[k][1]);
+                }
+            }
         }
-        st(out + c, v * inv);
     }
-    if (threadIdx.x == 0 && lse) lse[bh] = (mx + log2f(L)) * kLn2;
+    if (!active) return;
+#pragma unroll
+    for (int k = 0; k < kMaxCols; ++k) {
+        const int c = 2 * t + 256 * k;
+        if (c < d_c) st2(out + c, acc[k][0], acc[k][1]);
+    }
 }
 
 }  // namespace
@@ -271,13 +321,14 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
                          const void* sched, const float* part_o, const float* part_l, void* o_lat,
                          float* lse, cudaStream_t s) {
-    const int blocks = batch * d.n_heads;
+    if (d.d_c > 1024) return cudaErrorInvalidValue;
+    const dim3 grid(batch, (d.n_heads + 1) / 2);
     if (bf16)
-        merge_kernel<<<blocks, 128, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                            (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
+        merge_kernel<<<grid, 256, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                          (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
     else
-        merge_kernel<<<blocks, 128, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                            (float*)o_lat, lse, d.n_heads, d.d_c);
+        merge_kernel<<<grid, 256, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                          (float*)o_lat, lse, d.n_heads, d.d_c);
     note_launch();
     return cudaGetLastError();
 }

@@ -4,21 +4,28 @@
 // Work unit: a 2-CTA cluster walks one contiguous range of the flattened context
 // (same schedule as the CUDA-core kernel).  CTA r of the pair owns latent columns
 // [256r, 256r+256) and rotary columns [512+32r, 512+32r+32) of every cache row, so
-// the pair streams each row from HBM exactly once.  Per tile of 32 rows:
+// the pair streams each row from HBM exactly once.  Per tile of 64 rows:
 //
-//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=32 rows, K=288 (smem x smem -> TMEM)
-//   S   = S_0 + S_1          each CTA sends its fp32 partial to the peer through DSMEM
+//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=64 rows, K=288; Q'_r is the A
+//                            operand in tensor memory, the cache tile the B operand
+//   S   = S_0 + S_1          each CTA sends its fp32 partial to the peer (DSMEM)
 //   P   = exp2(S - m)        online softmax (identical in both CTAs; lazy max update)
-//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=32 (cache tile as MN-major B)
+//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=64; P (bf16) in tensor memory,
+//                            the cache tile read again as an MN-major B operand
 //
-// O_r (128 x 256 fp32) lives in TMEM for the whole range; four score tiles rotate
-// through TMEM.  Warp roles: warp 0 TMA producer, warp 1 MMA issuer (score MMAs two
-// tiles ahead of the value MMA), warp 2 TMEM owner, warps 4-7 softmax/exchange/
-// epilogue (thread i <-> head i <-> TMEM lane i), which fetch and send the next
-// tile's partial scores before working on the current one.  The exchange uses
-// st.async with the peer's mbarrier counting the bytes, so it needs no fences.
-// Every wait is bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains
-// its own in-flight copies and MMAs, frees TMEM and returns.
+// Tensor memory (512 columns): O_r 128 x 256 fp32, Q'_r 128 x 288 bf16 (144 columns),
+// S 128 x 64 fp32, P 128 x 64 bf16 (32 columns).  Shared memory holds only the
+// 4-stage ring of cache tiles and two exchange buffers, so each CTA keeps about
+// 100 KB of cache in flight.
+//
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (the score MMA of tile T+1 is
+// issued before the value MMA of tile T), warp 2 TMEM owner, warps 4-7 softmax and
+// exchange (thread i <-> head i <-> TMEM lane i), warps 8-11 load Q' of each piece
+// into tensor memory and write each piece's output.  The exchange buffer is laid out
+// [16-byte chunk][head], so the 32 lanes of a warp write 512 contiguous bytes into
+// the peer (whole 32-byte sectors on the cluster interconnect); the peer's mbarrier
+// counts the bytes.  Every wait is bounded in time; on expiry the CTA raises
+// MLA_DEV_TIMEOUT, drains its own in-flight copies and MMAs, frees TMEM and returns.
 #include <mutex>
 
 #include "mla_common.cuh"
@@ -32,16 +39,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTok = 32;              // cache rows per tile
+constexpr int kTok = 64;              // cache rows per tile (score MMA N, value MMA K)
 constexpr int kStages = 4;            // TMA ring depth
-constexpr int kSBuf = 4;              // score tiles in TMEM (score MMA runs 2 tiles ahead)
-constexpr int kXBuf = 4;              // exchange buffers (the peer writes up to 3 tiles ahead)
-constexpr int kMmaLead = 2;           // score MMAs issued ahead of the value MMA
-// Value-MMA completion is tracked per tile slot T % kODone.  When tile T's scores are
-// fetched, the value MMA of tile T-3 has completed (it was issued before the score
-// MMA of T), so a slot is never more than one phase behind when it is waited on.
-constexpr int kODone = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kHeads = 128;           // MMA M (heads beyond n_heads are computed and dropped)
 constexpr int kLatHalf = 256;         // latent columns per CTA
 constexpr int kRopeHalf = 32;         // rotary columns per CTA
@@ -49,38 +49,35 @@ constexpr int kRowElems = 576;        // d_c + d_r
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // shared memory layout (byte offsets from a 1024-aligned base)
-constexpr uint32_t kQBox = kHeads * 128;                 // 128 rows x 64 bf16, 128B swizzle
-constexpr uint32_t kQRope = kHeads * 64;                 // 128 rows x 32 bf16, 64B swizzle
-constexpr uint32_t kQBytes = 4 * kQBox + kQRope;         // 73728
-constexpr uint32_t kTBox = kTok * 128;                   // 32 rows x 64 bf16
-constexpr uint32_t kTRope = kTok * 64;                   // 32 rows x 32 bf16
-constexpr uint32_t kStageBytes = 4 * kTBox + kTRope;     // 18432
-constexpr uint32_t kPBytes = kHeads * kTok * 2;          // P tile, bf16, 64B swizzle
-constexpr uint32_t kXBytes = kHeads * kTok * 4;          // peer's fp32 partial scores
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffStage = kOffQ + kQBytes;
-constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffX = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffBar = kOffX + kXBuf * kXBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;   // barriers/flags + alignment slack
+constexpr uint32_t kTBox = kTok * 128;                   // 64 rows x 64 bf16, 128B swizzle
+constexpr uint32_t kTRope = kTok * 64;                   // 64 rows x 32 bf16, 64B swizzle
+constexpr uint32_t kStageBytes = 4 * kTBox + kTRope;     // 36864
+constexpr uint32_t kXBytes = kHeads * kTok * 4;          // the peer's fp32 partial scores
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
+constexpr uint32_t kOffStats = kOffX + 2 * kXBytes;      // [piece parity][m, l][head] fp32
+constexpr uint32_t kOffBar = kOffStats + 2 * 2 * kHeads * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers/flags + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier indices
 enum : int {
-    B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
-    B_SEMPTY = B_SFULL + kSBuf, B_PFULL = B_SEMPTY + kSBuf, B_PEMPTY = B_PFULL + 2,
-    B_ODONE = B_PEMPTY + 2, B_OFREE = B_ODONE + kODone, B_XFULL, B_FIN = B_XFULL + kXBuf, B_COUNT
+    B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL, B_SEMPTY,
+    B_PFULL, B_VDONE, B_OFREE, B_XFULL, B_STATS = B_XFULL + 2, B_FIN, B_COUNT
 };
-static_assert(B_COUNT * 8 <= 448, "barrier area");
-constexpr uint32_t kOffTslot = kOffBar + 448;
-constexpr uint32_t kOffAbort = kOffBar + 452;
+static_assert(B_COUNT * 8 <= 240, "barrier area");
+constexpr uint32_t kOffTslot = kOffBar + 240;
+constexpr uint32_t kOffAbort = kOffBar + 244;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;          // O_r: 256 columns
-constexpr uint32_t kColS = 256;        // S: kSBuf x 32 columns
+constexpr uint32_t kColO = 0;          // O_r: 256 fp32 columns
+constexpr uint32_t kColQ = 256;        // Q'_r: 288 bf16 = 144 columns
+constexpr uint32_t kColS = 416;        // S: 64 fp32 columns
+constexpr uint32_t kColP = 480;        // P: 64 bf16 = 32 columns
 
 struct TcArgs {
+    const __nv_bfloat16* qp;           // folded queries [batch * n_h, 576]
     const int64_t* row_off;
     const int64_t* cum;
     const Schedule* sched;
@@ -136,6 +133,8 @@ struct SegWalk {
     }
 };
 
+__device__ __forceinline__ int tiles_of(const Seg& s) { return (int)((s.hi - s.lo + kTok - 1) / kTok); }
+
 // The worker's tiles in order: global tile index T, piece index si, tile t of ntiles.
 struct TileIt {
     SegWalk walk;
@@ -148,7 +147,7 @@ struct TileIt {
         ++si;
         ++T;
         t = 0;
-        ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
+        ntiles = tiles_of(seg);
         return true;
     }
     __device__ bool first_tile() const { return t == 0; }
@@ -180,8 +179,7 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c
     }
 }
 
-// Warp-uniform form for the softmax warps: tcgen05.ld/st and warp votes need all 32
-// lanes on the same path, so a lane that gives up makes the whole warp give up.
+// Warp-uniform form for warps that issue tcgen05.ld/st (all 32 lanes on one path).
 template <bool kCluster>
 __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, const Ctl& c) {
     const bool ok = wait<kCluster>(bar, parity, c);
@@ -197,12 +195,11 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return smem_desc(a, 16, 1024, kSwizzle128B); }
 __device__ __forceinline__ uint64_t kdesc64(uint32_t a) { return smem_desc(a, 16, 512, kSwizzle64B); }
-// MN-major 128B-swizzled B: 64-column atoms 4096 B apart (one TMA box), 8-row groups 1024 B apart.
+// MN-major 128B-swizzled B: 64-column atoms one TMA box (kTBox bytes) apart, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return smem_desc(a, kTBox, 1024, kSwizzle128B); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
-                const __grid_constant__ CUtensorMap map_q128, const __grid_constant__ CUtensorMap map_q64,
                 TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -211,9 +208,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     if ((int64_t)g * S.per >= S.total) return;          // both CTAs of the pair leave together
 
     const uint32_t base = smem_addr(sm);
-    const uint32_t sQ = base + kOffQ, sStage = base + kOffStage, sP = base + kOffP, sX = base + kOffX;
+    const uint32_t sStage = base + kOffStage, sX = base + kOffX;
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
     uint32_t* tslot = (uint32_t*)(sm + kOffTslot);
+    float* stats = (float*)(sm + kOffStats);
     volatile int* abort_flag = (volatile int*)(sm + kOffAbort);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -223,13 +221,15 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
-        mbar_init(bar(B_QFULL), 1);
+        mbar_init(bar(B_QFULL), 128);
         mbar_init(bar(B_QEMPTY), 1);
-        for (int i = 0; i < kSBuf; ++i) { mbar_init(bar(B_SFULL + i), 1); mbar_init(bar(B_SEMPTY + i), 128); }
-        for (int i = 0; i < 2; ++i) { mbar_init(bar(B_PFULL + i), 128); mbar_init(bar(B_PEMPTY + i), 1); }
-        for (int i = 0; i < kXBuf; ++i) mbar_init(bar(B_XFULL + i), 1);
-        for (int i = 0; i < kODone; ++i) mbar_init(bar(B_ODONE + i), 1);
+        mbar_init(bar(B_SFULL), 1);
+        mbar_init(bar(B_SEMPTY), 128);
+        mbar_init(bar(B_PFULL), 128);
+        mbar_init(bar(B_VDONE), 1);
         mbar_init(bar(B_OFREE), 128);
+        for (int i = 0; i < 2; ++i) mbar_init(bar(B_XFULL + i), 1);
+        mbar_init(bar(B_STATS), 128);
         mbar_init(bar(B_FIN), 1);
         *abort_flag = 0;
         fence_mbar_init_cluster();
@@ -239,8 +239,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&map_c128); prefetch_tmap(&map_c64);
-        prefetch_tmap(&map_q128); prefetch_tmap(&map_q64);
+        prefetch_tmap(&map_c128);
+        prefetch_tmap(&map_c64);
     }
     tc_fence_before();
     cluster_sync();                 // barriers of both CTAs initialised before any remote signal
@@ -250,40 +250,25 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            SegWalk walk;
-            walk.init(a.cum, a.batch, g, S.per, S.total);
-            Seg seg;
-            uint32_t T = 0, si = 0;
-            bool ok = true;
-            while (ok && walk.next(seg)) {
-                ok = wait<false>(bar(B_QEMPTY), (si & 1) ^ 1, ctl);
-                if (!ok) break;
-                mbar_expect_tx(bar(B_QFULL), kQBytes);
-                const int qy = seg.b * a.n_h;
+            TileIt it;
+            it.walk.init(a.cum, a.batch, g, S.per, S.total);
+            uint32_t issued = 0;
+            while (it.next()) {
+                const uint32_t T = it.T, st = T % kStages;
+                if (!wait<false>(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1, ctl)) break;
+                const uint32_t dst = sStage + st * kStageBytes;
+                const int y = (int)(a.row_off[it.seg.b] + it.seg.lo + (int64_t)it.t * kTok);
+                mbar_expect_tx(bar(B_FULL + st), kStageBytes);
                 for (int j = 0; j < 4; ++j)
-                    tma_load_2d(sQ + j * kQBox, &map_q128, rank * kLatHalf + 64 * j, qy, bar(B_QFULL));
-                tma_load_2d(sQ + 4 * kQBox, &map_q64, 512 + rank * kRopeHalf, qy, bar(B_QFULL));
-                ++si;
-                const int64_t row0 = a.row_off[seg.b] + seg.lo;
-                const int ntiles = (int)((seg.hi - seg.lo + kTok - 1) / kTok);
-                for (int t = 0; t < ntiles; ++t, ++T) {
-                    const uint32_t st = T % kStages;
-                    ok = wait<false>(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1, ctl);
-                    if (!ok) break;
-                    const uint32_t dst = sStage + st * kStageBytes;
-                    const int y = (int)(row0 + (int64_t)t * kTok);
-                    mbar_expect_tx(bar(B_FULL + st), kStageBytes);
-                    for (int j = 0; j < 4; ++j)
-                        tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
-                    tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
-                }
+                    tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
+                tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
+                issued = T + 1;
             }
             // drain: every copy this thread issued has landed before the CTA may exit
-            for (uint32_t k = 0; k < kStages && k < T; ++k) {
-                const uint32_t Tk = T - 1 - k;
+            for (uint32_t k = 0; k < kStages && k < issued; ++k) {
+                const uint32_t Tk = issued - 1 - k;
                 drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
             }
-            if (si > 0) drain(bar(B_QFULL), (si - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -295,107 +280,102 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             pv.walk.init(a.cum, a.batch, g, S.per, S.total);
             bool ok = true;
             auto issue_score = [&]() -> bool {
-                const uint32_t T = sc.T, st = T % kStages, sb = T % kSBuf;
+                const uint32_t T = sc.T, st = T % kStages;
                 if (sc.first_tile() && !wait<false>(bar(B_QFULL), sc.si & 1, ctl)) return false;
                 if (!wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl)) return false;
-                if (!wait<false>(bar(B_SEMPTY + sb), ((T / kSBuf) & 1) ^ 1, ctl)) return false;
+                if (T > 0 && !wait<false>(bar(B_SEMPTY), (T - 1) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t stage = sStage + st * kStageBytes;
-                const uint32_t d = tmem + kColS + sb * kTok;
-                for (int j = 0; j < 4; ++j)
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(d, kdesc128(sQ + j * kQBox + 32 * k), kdesc128(stage + j * kTBox + 32 * k),
-                                 id_s, (j | k) ? 1u : 0u);
-                for (int k = 0; k < 2; ++k)
-                    mma_bf16(d, kdesc64(sQ + 4 * kQBox + 32 * k), kdesc64(stage + 4 * kTBox + 32 * k), id_s, 1u);
-                mma_commit(bar(B_SFULL + sb));
+                const uint32_t d = tmem + kColS;
+                for (int kk = 0; kk < 16; ++kk)
+                    mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
+                                id_s, kk ? 1u : 0u);
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_bf16_ts(d, tmem + kColQ + 8 * (16 + kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
+                mma_commit(bar(B_SFULL));
                 if (sc.last_tile()) mma_commit(bar(B_QEMPTY));
                 return true;
             };
             auto issue_value = [&]() -> bool {
-                const uint32_t T = pv.T, st = T % kStages, pb = T & 1;
-                if (!wait<false>(bar(B_PFULL + pb), (T >> 1) & 1, ctl)) return false;
+                const uint32_t T = pv.T, st = T % kStages;
+                if (!wait<false>(bar(B_PFULL), T & 1, ctl)) return false;
                 if (pv.first_tile() && pv.si > 0 && !wait<false>(bar(B_OFREE), (pv.si - 1) & 1, ctl)) return false;
                 tc_fence_after();
                 const uint32_t stage = sStage + st * kStageBytes;
                 for (int k = 0; k < kTok / 16; ++k)
-                    mma_bf16(tmem + kColO, kdesc64(sP + pb * kPBytes + 32 * k), mndesc128(stage + 2048 * k),
-                             id_o, (pv.first_tile() && k == 0) ? 0u : 1u);
+                    mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, mndesc128(stage + 2048 * k), id_o,
+                                (pv.first_tile() && k == 0) ? 0u : 1u);
                 mma_commit(bar(B_EMPTY + st));
-                mma_commit(bar(B_PEMPTY + pb));
-                mma_commit(bar(B_ODONE + T % kODone));
+                mma_commit(bar(B_VDONE));
                 return true;
             };
+            // Order: score(T+1) before value(T), so the next scores are computed while the
+            // softmax of tile T runs -- except when tile T+1 opens a new piece: its score
+            // MMA waits for that piece's Q', and value(T) (which the piece's epilogue
+            // waits for) must not queue behind that load.
             bool more = sc.next();
-            for (int k = 0; k < kMmaLead && more && ok; ++k) {
+            if (more) {
                 ok = issue_score();
                 more = sc.next();
             }
             while (ok && pv.next()) {
-                if (more) {
+                const bool early = more && !sc.first_tile();
+                if (early) {
                     ok = issue_score();
                     more = sc.next();
                     if (!ok) break;
                 }
                 ok = issue_value();
+                if (ok && more && !early) {
+                    ok = issue_score();
+                    more = sc.next();
+                }
             }
             mma_commit(bar(B_FIN));
             drain(bar(B_FIN), 0);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax / exchange / epilogue
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ softmax / exchange
         const int i = tid - 128;                        // head row == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t peer_x = mapa(sX, peer);
         const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
-        const uint32_t xrow = (uint32_t)i * (kTok * 4);   // this row's 128 bytes in an X buffer
-        TileIt fe, co;                                  // fetch/send position, consume position
-        fe.walk.init(a.cum, a.batch, g, S.per, S.total);
+        TileIt co;
         co.walk.init(a.cum, a.batch, g, S.per, S.total);
         bool ok = true;
-        float s_cur[kTok], s_nxt[kTok];
-        // take this CTA's partial scores of tile fe.T out of TMEM and send them to the peer
-        auto fetch_send = [&](float (&s)[kTok]) -> bool {
-            const uint32_t T = fe.T, sb = T % kSBuf, xb = T % kXBuf;
-            if (!wwait<false>(bar(B_SFULL + sb), (T / kSBuf) & 1, ctl)) return false;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + kColS + sb * kTok, s);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(B_SEMPTY + sb));
-            if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);     // the peer's copy of tile T
-#pragma unroll
-            for (int c = 0; c < kTok / 4; ++c) {
-                const uint32_t off = xb * kXBytes + xrow + (uint32_t)((c ^ (i & 7)) * 16);
-                st_async_v4(peer_x + off, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], peer_xfull + 8 * xb);
-            }
-            return true;
-        };
-        bool more = fe.next();
-        if (more) { ok = fetch_send(s_cur); more = fe.next(); }
         float m_run = -INFINITY, l_run = 0.f;
         while (ok && co.next()) {
-            const uint32_t T = co.T, pb = T & 1, xb = T % kXBuf, st = T % kStages;
-            if (more) {
-                if (!(ok = fetch_send(s_nxt))) break;
-                more = fe.next();
-            }
+            const uint32_t T = co.T, xb = T & 1, st = T % kStages;
+            // this CTA's partial scores: out of TMEM, then to the peer
+            float s[kTok];
+            if (!(ok = wwait<false>(bar(B_SFULL), T & 1, ctl))) break;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
+            tmem_ld32(tmem + lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(B_SEMPTY));
+            if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
+#pragma unroll
+            for (int c = 0; c < kTok / 4; ++c)
+                st_async_v4(peer_x + xb * kXBytes + (uint32_t)(c * kHeads + i) * 16, s[4 * c], s[4 * c + 1],
+                            s[4 * c + 2], s[4 * c + 3], peer_xfull + 8 * xb);
             if (co.first_tile()) { m_run = -INFINITY; l_run = 0.f; }
             // add the peer's partial scores of tile T
-            if (!(ok = wwait<true>(bar(B_XFULL + xb), (T / kXBuf) & 1, ctl))) break;
-            const uint8_t* xr = sm + kOffX + xb * kXBytes + xrow;
+            if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
+            const float4* xr = reinterpret_cast<const float4*>(sm + kOffX + xb * kXBytes) + i;
 #pragma unroll
             for (int c = 0; c < kTok / 4; ++c) {
-                const float4 v = *(const float4*)(xr + ((c ^ (i & 7)) * 16));
-                s_cur[4 * c] += v.x; s_cur[4 * c + 1] += v.y; s_cur[4 * c + 2] += v.z; s_cur[4 * c + 3] += v.w;
+                const float4 v = xr[c * kHeads];
+                s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
             }
             // rows past the end of this piece do not count
             const int valid = co.valid_rows();
             float mt = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kTok; ++j) {
-                if (j >= valid) s_cur[j] = -INFINITY;
-                mt = fmaxf(mt, s_cur[j]);
+                if (j >= valid) s[j] = -INFINITY;
+                mt = fmaxf(mt, s[j]);
             }
             // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
             const bool need = mt > m_run + 8.f;
@@ -405,9 +385,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 m_run = mt;
                 l_run *= alpha;
             }
-            if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
-                if (!(ok = wwait<false>(bar(B_ODONE + (T - 1) % kODone), ((T - 1) / kODone) & 1, ctl))) break;
+            // the value MMA of the previous tile has finished with P and O
+            if (T > 0) {
+                if (!(ok = wwait<false>(bar(B_VDONE), (T - 1) & 1, ctl))) break;
                 tc_fence_after();
+            }
+            if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
                 for (int c = 0; c < kLatHalf / 32; ++c) {
                     float o[32];
                     tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
@@ -416,23 +399,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     for (int j = 0; j < 32; ++j) o[j] *= alpha;
                     tmem_st32(tmem + lane_base + kColO + 32 * c, o);
                 }
-                tmem_wait_st();
             }
             // P tile (bf16) for the value MMA; the sum uses the rounded values
-            if (!(ok = wwait<false>(bar(B_PEMPTY + pb), ((T >> 1) & 1) ^ 1, ctl))) break;
             uint32_t packed[kTok / 2];
 #pragma unroll
             for (int j = 0; j < kTok / 2; ++j) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s_cur[2 * j] - m_run),
-                                                                exp2f(s_cur[2 * j + 1] - m_run));
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_run),
+                                                                exp2f(s[2 * j + 1] - m_run));
                 l_run += __low2float(h2) + __high2float(h2);
                 packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            uint8_t* prow = sm + kOffP + pb * kPBytes + i * 64;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                *(uint4*)(prow + ((c ^ ((i >> 1) & 3)) * 16)) =
-                    make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            tmem_st32u(tmem + lane_base + kColP, packed);
             if (valid < kTok) {
                 // the value MMA must not see rows of the tile beyond the piece (they may
                 // hold anything): zero them in this CTA's latent half of the stage
@@ -441,28 +418,92 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
                     *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL + pb));
-#pragma unroll
-            for (int j = 0; j < kTok; ++j) s_cur[j] = s_nxt[j];
-            if (!co.last_tile()) continue;
-            // epilogue of this piece: O_r / l, log2-sum-exp
-            if (!(ok = wwait<false>(bar(B_ODONE + T % kODone), (T / kODone) & 1, ctl))) break;
-            tc_fence_after();
-            const float inv = 1.f / l_run;
-            const float lse2 = m_run + log2f(l_run);
+            mbar_arrive(bar(B_PFULL));
+            if (co.last_tile()) {
+                float* sp = stats + (co.si & 1) * 2 * kHeads;
+                sp[i] = m_run;
+                sp[kHeads + i] = l_run;
+                mbar_arrive(bar(B_STATS));
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ Q' loader / epilogue
+        const int i = tid - 256;                        // head row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        SegWalk walk;
+        walk.init(a.cum, a.batch, g, S.per, S.total);
+        Seg cur, nxt;
+        bool have = walk.next(cur);
+        uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
+        // Q' of one piece into TMEM columns kColQ.. (zero rows for heads >= n_h)
+        auto load_q = [&](const Seg& sg) {
             const bool row_ok = i < a.n_h;
-            const Seg& seg = co.seg;
+            const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
+            const uint4 zero = make_uint4(0, 0, 0, 0);
+            {   // latent columns [256r, 256r + 128)
+                uint32_t r[2][32];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_ok ? src[rank * 32 + c] : zero;
+                    r[c >> 3][4 * (c & 7)] = v.x; r[c >> 3][4 * (c & 7) + 1] = v.y;
+                    r[c >> 3][4 * (c & 7) + 2] = v.z; r[c >> 3][4 * (c & 7) + 3] = v.w;
+                }
+                tmem_st32u(tmem + lane_base + kColQ, r[0]);
+                tmem_st32u(tmem + lane_base + kColQ + 32, r[1]);
+            }
+            {   // latent columns [256r + 128, 256r + 256) and rotary [512 + 32r, +32)
+                uint32_t r[2][32], q[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 v = row_ok ? src[rank * 32 + 16 + c] : zero;
+                    r[c >> 3][4 * (c & 7)] = v.x; r[c >> 3][4 * (c & 7) + 1] = v.y;
+                    r[c >> 3][4 * (c & 7) + 2] = v.z; r[c >> 3][4 * (c & 7) + 3] = v.w;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = row_ok ? src[64 + rank * 4 + c] : zero;
+                    q[4 * c] = v.x; q[4 * c + 1] = v.y; q[4 * c + 2] = v.z; q[4 * c + 3] = v.w;
+                }
+                tmem_st32u(tmem + lane_base + kColQ + 64, r[0]);
+                tmem_st32u(tmem + lane_base + kColQ + 96, r[1]);
+                tmem_st16(tmem + lane_base + kColQ + 128, q);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_QFULL));
+        };
+        bool ok = true;
+        if (have) load_q(cur);
+        while (ok && have) {
+            t_end += (uint32_t)tiles_of(cur);
+            const bool more = walk.next(nxt);
+            if (more) {
+                // the score MMAs of this piece are done with Q'
+                if (!(ok = wwait<false>(bar(B_QEMPTY), si & 1, ctl))) break;
+                tc_fence_after();
+                load_q(nxt);
+            }
+            // epilogue of this piece: O_r / l, log2-sum-exp
+            if (!(ok = wwait<false>(bar(B_STATS), si & 1, ctl))) break;
+            const float* sp = stats + (si & 1) * 2 * kHeads;
+            const float m_fin = sp[i], l_fin = sp[kHeads + i];
+            if (!(ok = wwait<false>(bar(B_VDONE), (t_end - 1) & 1, ctl))) break;
+            tc_fence_after();
+            const float inv = 1.f / l_fin;
+            const float lse2 = m_fin + log2f(l_fin);
+            const bool row_ok = i < a.n_h;
             for (int c = 0; c < kLatHalf / 32; ++c) {
                 float o[32];
                 tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
                 tmem_wait_ld();
                 if (!row_ok) continue;
                 const int col = (int)rank * kLatHalf + 32 * c;
-                if (seg.complete) {
-                    __nv_bfloat16* dst = a.o_lat + ((int64_t)seg.b * a.n_h + i) * 512 + col;
+                if (cur.complete) {
+                    __nv_bfloat16* dst = a.o_lat + ((int64_t)cur.b * a.n_h + i) * 512 + col;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t w[4];
@@ -474,7 +515,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         *(uint4*)(dst + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 } else {
-                    float* dst = a.part_o + (seg.slot * a.n_h + i) * 512 + col;
+                    float* dst = a.part_o + (cur.slot * a.n_h + i) * 512 + col;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         *(float4*)(dst + 4 * q) = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
@@ -482,11 +523,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 }
             }
             if (row_ok && rank == 0) {
-                if (seg.complete) { if (a.lse) a.lse[(int64_t)seg.b * a.n_h + i] = lse2 * kLn2; }
-                else a.part_l[seg.slot * a.n_h + i] = lse2;
+                if (cur.complete) { if (a.lse) a.lse[(int64_t)cur.b * a.n_h + i] = lse2 * kLn2; }
+                else a.part_l[cur.slot * a.n_h + i] = lse2;
             }
             tc_fence_before();
             mbar_arrive(bar(B_OFREE));
+            cur = nxt;
+            have = more;
+            ++si;
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -539,20 +583,19 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             void* o_lat, float* lse, float* part_o, float* part_l,
                             int32_t* dev_status, cudaStream_t s) {
+    (void)q_rows;
     if (!get_encoder()) return cudaErrorNotSupported;
-    CUtensorMap mc128, mc64, mq128, mq64;
+    CUtensorMap mc128, mc64;
     if (!encode_2d(&mc128, cache, kRowElems, (uint64_t)cache_rows, 64, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !encode_2d(&mq128, qp, kRowElems, (uint64_t)q_rows, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mq64, qp, kRowElems, (uint64_t)q_rows, 32, kHeads, CU_TENSOR_MAP_SWIZZLE_64B))
+        !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    TcArgs a{row_off, cum, (const Schedule*)sched, (__nv_bfloat16*)o_lat, lse, part_o, part_l, dev_status,
-             d.n_heads, batch};
+    TcArgs a{(const __nv_bfloat16*)qp, row_off, cum, (const Schedule*)sched, (__nv_bfloat16*)o_lat, lse,
+             part_o, part_l, dev_status, d.n_heads, batch};
     cudaError_t e = cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     profile_before_split(s);
-    split_tc_kernel<<<dim3(2 * workers), dim3(kThreads), kSmemBytes, s>>>(mc128, mc64, mq128, mq64, a);
+    split_tc_kernel<<<dim3(2 * workers), dim3(kThreads), kSmemBytes, s>>>(mc128, mc64, a);
     profile_after_split(s);
     note_launch();
     return cudaGetLastError();

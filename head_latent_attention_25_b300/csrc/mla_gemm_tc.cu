@@ -196,38 +196,47 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
 }
 
-// cache row = [sum of partials for c ; RoPE(sum of partials for k_R, pos)] in bf16
-__global__ void append_finalize_kernel(const float* part, int k_splits, int n_tok, int n_new,
-                                       int d_c, int d_r, float rope_base, const int64_t* row_off,
-                                       const int32_t* cap, const int32_t* pos0, int64_t cache_rows,
-                                       __nv_bfloat16* cache, int32_t* dev_status) {
+// cache row = [sum of partials for c ; RoPE(sum of partials for k_R, pos)] in bf16.
+// Grid (token, pair groups of kFinPairs): thread <-> one pair (2e, 2e+1) of one row,
+// which also keeps a rotary pair in one thread.  The split partials are added in
+// split order (fixed, so the result does not depend on timing); the loads of the
+// unrolled loop are independent, so several are in flight per thread.
+constexpr int kFinPairs = 128;
+
+__global__ void __launch_bounds__(kFinPairs)
+append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, int n_new, int d_c,
+                       int d_r, double rope_r, const int64_t* __restrict__ row_off,
+                       const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
+                       int64_t cache_rows, __nv_bfloat16* __restrict__ cache, int32_t* dev_status) {
     const int t = blockIdx.x;
-    if (t >= n_tok) return;
+    const int width = d_c + d_r;
+    const int e = 2 * (blockIdx.y * kFinPairs + threadIdx.x);
     const int b = t / n_new, j = t % n_new;
     const int p0 = pos0[b];
     const int64_t off = row_off[b], cp = cap[b];
     if (p0 < 0 || (int64_t)p0 + n_new > cp || off < 0 || off + cp > cache_rows) {
-        if (j == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
+        if (j == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
         return;
     }
+    if (e >= width) return;
     const int64_t pos = (int64_t)p0 + j;
-    const int width = d_c + d_r;
-    __nv_bfloat16* row = cache + (off + pos) * width;
-    for (int e = 2 * threadIdx.x; e < width; e += 2 * blockDim.x) {
-        float v0 = 0.f, v1 = 0.f;
-        for (int s = 0; s < k_splits; ++s) {
-            const float* p = part + ((int64_t)s * n_tok + t) * width + e;
-            v0 += p[0];
-            v1 += p[1];
-        }
-        if (e >= d_c) {
-            float c, sn;
-            rope_cos_sin(pos, (e - d_c) >> 1, d_r, rope_base, &c, &sn);
-            const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
-            v0 = r0; v1 = r1;
-        }
-        *(__nv_bfloat162*)(row + e) = __floats2bfloat162_rn(v0, v1);
+    const float* p = part + (int64_t)t * width + e;
+    const int64_t split_stride = (int64_t)n_tok * width;
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < k_splits; ++s) {
+        const float2 x = *reinterpret_cast<const float2*>(p + s * split_stride);
+        v0 += x.x;
+        v1 += x.y;
     }
+    if (e >= d_c) {
+        float c, sn;
+        rope_cos_sin(pos, (e - d_c) >> 1, rope_r, &c, &sn);
+        const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
+        v0 = r0;
+        v1 = r1;
+    }
+    *(__nv_bfloat162*)(cache + (off + pos) * width + e) = __floats2bfloat162_rn(v0, v1);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -348,9 +357,11 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
     a.dev_status = dev_status;
     cudaError_t e = run_gemm(ma, ma2, mb, a, 1, nt, s);
     if (e != cudaSuccess) return e;
-    append_finalize_kernel<<<n_tok, 128, 0, s>>>((const float*)workspace, splits, n_tok, n_new, d.d_c,
-                                                 d.d_r, d.rope_base, row_off, cap, pos0, cache_rows,
-                                                 (__nv_bfloat16*)cache, dev_status);
+    const dim3 fin_grid(n_tok, (width / 2 + kFinPairs - 1) / kFinPairs);
+    append_finalize_kernel<<<fin_grid, kFinPairs, 0, s>>>((const float*)workspace, splits, n_tok, n_new,
+                                                          d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
+                                                          row_off, cap, pos0, cache_rows,
+                                                          (__nv_bfloat16*)cache, dev_status);
     note_launch();
     return cudaGetLastError();
 }

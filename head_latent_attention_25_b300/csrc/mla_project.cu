@@ -23,7 +23,7 @@ struct GemmArgs {
     int32_t mode;
     // append epilogue
     int32_t n_new, d_c, d_r;
-    float rope_base;
+    double rope_r;
     const int64_t* row_off; const int32_t* cap; const int32_t* pos0; int32_t* dev_status;
     int64_t cache_rows;
 };
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(NT) gemm_xwt_kernel(GemmArgs a) {
             Tout* Y = (Tout*)a.y + (off + pos) * row_elems + n;
             if (n >= a.d_c) {            // k_R = RoPE(W_KR h, pos) on the pair (2k, 2k+1)
                 float c, s;
-                rope_cos_sin(pos, (n - a.d_c) >> 1, a.d_r, a.rope_base, &c, &s);
+                rope_cos_sin(pos, (n - a.d_c) >> 1, a.rope_r, &c, &s);
                 float r0 = v0 * c - v1 * s, r1 = v0 * s + v1 * c;
                 v0 = r0; v1 = r1;
             }
@@ -134,26 +134,33 @@ GemmArgs blank() {
 }
 
 // Q'[b, i, d_c + 2k .. 2k+1] = alpha * RoPE(q_R[b, i, :], seq_len[b] - 1) pair k.
-// One block per sequence: the d_r/2 angles are shared by all heads.
+// Grid (batch, head groups of kRopeHeads): the d_r/2 angles of a sequence are formed
+// once per block in shared memory and shared by its heads; every thread then turns
+// independent pairs (paired loads and stores, no dependence between iterations).
 constexpr int kMaxRopePairs = 512;
+constexpr int kRopeHeads = 16;
 
 template <typename Tin, typename Tout>
-__global__ void fold_rope_kernel(const Tin* q_r, const int32_t* seq_len, Tout* qp, int n_h, int d_c,
-                                 int d_r, float base, float alpha, int batch) {
+__global__ void __launch_bounds__(256) fold_rope_kernel(const Tin* __restrict__ q_r,
+                                                        const int32_t* __restrict__ seq_len,
+                                                        Tout* __restrict__ qp, int n_h, int d_c,
+                                                        int d_r, double rope_r, float alpha) {
     __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
     const int b = blockIdx.x;
-    if (b >= batch) return;
+    const int h0 = blockIdx.y * kRopeHeads;
     const int half = d_r / 2;
-    const int64_t pos = seq_len[b] > 0 ? (int64_t)seq_len[b] - 1 : 0;
-    for (int k = threadIdx.x; k < half; k += blockDim.x) rope_cos_sin(pos, k, d_r, base, &cs[k], &sn[k]);
+    const int n_heads = min(kRopeHeads, n_h - h0);
+    const int len = seq_len[b];
+    const int64_t pos = len > 0 ? (int64_t)len - 1 : 0;
+    for (int k = threadIdx.x; k < half; k += blockDim.x) rope_cos_sin(pos, k, rope_r, &cs[k], &sn[k]);
     __syncthreads();
-    for (int e = threadIdx.x; e < n_h * half; e += blockDim.x) {
-        const int i = e / half, k = e - i * half;
-        const Tin* src = q_r + ((int64_t)b * n_h + i) * d_r;
-        Tout* dst = qp + ((int64_t)b * n_h + i) * (d_c + d_r) + d_c;
-        const float x0 = ld(src + 2 * k), x1 = ld(src + 2 * k + 1);
-        st(dst + 2 * k, alpha * (x0 * cs[k] - x1 * sn[k]));
-        st(dst + 2 * k + 1, alpha * (x0 * sn[k] + x1 * cs[k]));
+    const int items = n_heads * half;
+#pragma unroll 4
+    for (int e = threadIdx.x; e < items; e += blockDim.x) {
+        const int i = h0 + e / half, k = e % half;
+        const float2 x = ld2(q_r + ((int64_t)b * n_h + i) * d_r + 2 * k);
+        st2(qp + ((int64_t)b * n_h + i) * (d_c + d_r) + d_c + 2 * k,
+            alpha * (x.x * cs[k] - x.y * sn[k]), alpha * (x.x * sn[k] + x.y * cs[k]));
     }
 }
 
@@ -170,7 +177,7 @@ cudaError_t launch_append(const mla_dims& d, bool bf16, int batch, int n_new, co
     a.w_g = 0; a.w_n = d.hidden; a.w_k = 1;
     a.y = cache;
     a.G = 1; a.M = batch * n_new; a.N = d.d_c + d.d_r; a.K = d.hidden;
-    a.mode = kAppend; a.n_new = n_new; a.d_c = d.d_c; a.d_r = d.d_r; a.rope_base = d.rope_base;
+    a.mode = kAppend; a.n_new = n_new; a.d_c = d.d_c; a.d_r = d.d_r; a.rope_r = rope_ratio(d.rope_base, d.d_r);
     a.row_off = row_off; a.cap = cap; a.pos0 = pos0; a.dev_status = dev_status;
     return dispatch(a, bf16, bf16, s);
 }
@@ -206,17 +213,19 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
 
 cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
                              const int32_t* seq_len, float alpha, void* qp, cudaStream_t s) {
-    const int blocks = batch, threads = 256;
+    if (d.d_r / 2 > kMaxRopePairs) return cudaErrorInvalidValue;
+    const dim3 grid(batch, (d.n_heads + kRopeHeads - 1) / kRopeHeads);
+    const double r = rope_ratio(d.rope_base, d.d_r);
     if (in_bf16) {
         if (out_bf16)
-            fold_rope_kernel<<<blocks, threads, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, d.rope_base, alpha, batch);
+            fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
+                (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, r, alpha);
         else
-            fold_rope_kernel<<<blocks, threads, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (float*)qp, d.n_heads, d.d_c, d.d_r, d.rope_base, alpha, batch);
+            fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
+                (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha);
     } else {
-        fold_rope_kernel<<<blocks, threads, 0, s>>>((const float*)q_r, seq_len, (float*)qp,
-            d.n_heads, d.d_c, d.d_r, d.rope_base, alpha, batch);
+        fold_rope_kernel<<<grid, 256, 0, s>>>((const float*)q_r, seq_len, (float*)qp,
+            d.n_heads, d.d_c, d.d_r, r, alpha);
     }
     note_launch();
     return cudaGetLastError();
