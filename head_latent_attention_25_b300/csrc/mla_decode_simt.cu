@@ -182,12 +182,13 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
 }
 
 // ------------------------------------------------------------------ merge
-// Grid (batch, head pairs): each half of the block (128 threads) merges one head of a
-// sequence that was cut across workers.  Pass 1 finds the maximum and the sum of the
-// pieces' log2-sum-exps (lanes stride over the pieces); pass 2 forms the normalised
-// piece weights in shared memory, 256 pieces at a time, and every thread adds its
-// two columns of all pieces with independent paired loads.
-constexpr int kMergeChunk = 256;
+// Grid (batch, head groups of 8): warp w of a block merges head 8*blockIdx.y + w of a
+// sequence that was cut across workers.  Lane j keeps the log2-sum-exps of pieces
+// j, j+32, ... in registers (one load round), the warp reduces their maximum and sum
+// with shuffles, and each piece's weight is broadcast from its lane while every lane
+// adds its 16 columns of that piece (4 float4 loads, a warp reads 2 KB contiguously).
+constexpr int kMergeHeads = 8;
+constexpr int kMergeRegs = 4;                   // pieces held per lane before the slow path
 
 __device__ __forceinline__ int64_t piece_slot(int64_t w, int64_t seq_begin, int64_t per) {
     // the worker's first segment (slot 2w) unless the sequence starts inside its range
@@ -195,77 +196,85 @@ __device__ __forceinline__ int64_t piece_slot(int64_t w, int64_t seq_begin, int6
 }
 
 template <typename Tout>
-__global__ void __launch_bounds__(256) merge_kernel(const int64_t* __restrict__ cum,
-                                                    const Schedule* __restrict__ sched,
-                                                    const float* __restrict__ part_o,
-                                                    const float* __restrict__ part_l,
-                                                    Tout* __restrict__ o_lat, float* __restrict__ lse,
-                                                    int n_h, int d_c) {
-    __shared__ float wts[2][kMergeChunk];
-    __shared__ float stat[2][2];
+__global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* __restrict__ cum,
+                                                                 const Schedule* __restrict__ sched,
+                                                                 const float* __restrict__ part_o,
+                                                                 const float* __restrict__ part_l,
+                                                                 Tout* __restrict__ o_lat,
+                                                                 float* __restrict__ lse, int n_h, int d_c) {
     const int b = blockIdx.x;
-    const int half = threadIdx.x >> 7, t = threadIdx.x & 127;
-    const int lane = t & 31, warp_in_half = t >> 5;
-    const int h = blockIdx.y * 2 + half;
-    const bool active = h < n_h;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y * kMergeHeads + (threadIdx.x >> 5);
+    if (h >= n_h) return;
     const int64_t seq0 = cum[b], seq1 = cum[b + 1];
-    Tout* out = o_lat + ((int64_t)b * n_h + (active ? h : 0)) * d_c;
+    const int64_t per = sched->per;
+    Tout* out = o_lat + ((int64_t)b * n_h + h) * d_c;
     if (seq1 == seq0) {                         // empty or rejected by the schedule
-        if (active) {
-            for (int c = 2 * t; c < d_c; c += 256) st2(out + c, 0.f, 0.f);
-            if (t == 0 && lse) lse[(int64_t)b * n_h + h] = -INFINITY;
-        }
+        for (int c = 2 * lane; c < d_c; c += 64) st2(out + c, 0.f, 0.f);
+        if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = -INFINITY;
         return;
     }
-    const int64_t per = sched->per;
     const int64_t first_w = seq0 / per, last_w = (seq1 - 1) / per;
     if (first_w == last_w) return;              // finished in place by its only worker
     const int64_t np = last_w - first_w + 1;
-    if (active && warp_in_half == 0) {
-        float mx = -INFINITY;
-        for (int64_t p = lane; p < np; p += 32)
-            mx = fmaxf(mx, part_l[piece_slot(first_w + p, seq0, per) * n_h + h]);
-        mx = warp_max(mx);
-        float L = 0.f;
-        for (int64_t p = lane; p < np; p += 32)
-            L += exp2f(part_l[piece_slot(first_w + p, seq0, per) * n_h + h] - mx);
-        L = warp_sum(L);
-        if (lane == 0) { stat[half][0] = mx; stat[half][1] = 1.f / L; }
-        if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
-    }
-    __syncthreads();
-    const float mx = stat[half][0], inv = stat[half][1];
-    // each thread owns columns 2t + 256k
-    constexpr int kMaxCols = 4;                 // d_c <= 1024 columns per head
-    float acc[kMaxCols][2] = {};
-    for (int64_t p0 = 0; p0 < np; p0 += kMergeChunk) {
-        const int nc = (int)min((int64_t)kMergeChunk, np - p0);
-        __syncthreads();
-        if (active)
-            for (int p = t; p < nc; p += 128)
-                wts[half][p] = exp2f(part_l[piece_slot(first_w + p0 + p, seq0, per) * n_h + h] - mx) * inv;
-        __syncthreads();
-        if (!active) continue;
-#pragma unroll 4
-        for (int p = 0; p < nc; ++p) {
-            const float wp = wts[half][p];
-            const float* src = part_o + (piece_slot(first_w + p0 + p, seq0, per) * n_h + h) * d_c;
+    // pass 1: maximum and sum of the pieces' log2-sum-exps
+    float lr[kMergeRegs];
+    float mx = -INFINITY;
 #pragma unroll
-            for (int k = 0; k < kMaxCols; ++k) {
-                const int c = 2 * t + 256 * k;
-                if (c < d_c) {
-                    const float2 v = *reinterpret_cast<const float2*>(src + c);
-                    acc[k][0] = fmaf(wp, v.x, acc[k][0]);
-                    acc[k][1] = fmaf(wp, v.y, acc[k][1]);
+    for (int k = 0; k < kMergeRegs; ++k) {
+        const int64_t p = lane + 32 * k;
+        lr[k] = p < np ? part_l[piece_slot(first_w + p, seq0, per) * n_h + h] : -INFINITY;
+        mx = fmaxf(mx, lr[k]);
+    }
+    for (int64_t p = lane + 32 * kMergeRegs; p < np; p += 32)
+        mx = fmaxf(mx, part_l[piece_slot(first_w + p, seq0, per) * n_h + h]);
+    mx = warp_max(mx);
+    float L = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMergeRegs; ++k) L += exp2f(lr[k] - mx);
+    for (int64_t p = lane + 32 * kMergeRegs; p < np; p += 32)
+        L += exp2f(part_l[piece_slot(first_w + p, seq0, per) * n_h + h] - mx);
+    L = warp_sum(L);
+    const float inv = 1.f / L;
+    if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
+    // pass 2: lane owns columns [16 lane, 16 lane + 16) (+ 512 k for wider latents)
+    constexpr int kCols = 16;
+    const bool vec = (d_c % kCols) == 0;        // float4 loads stay aligned
+    for (int c0 = kCols * lane; c0 < d_c + 31 * kCols; c0 += 32 * kCols) {
+        // every lane runs the loop the same number of times (the shuffles need all 32)
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+        const int nc = max(0, min(kCols, d_c - c0));
+        auto add_piece = [&](int64_t p, float lp) {
+            const float wp = exp2f(lp - mx) * inv;
+            const float* src = part_o + (piece_slot(first_w + p, seq0, per) * n_h + h) * d_c + c0;
+            if (vec && nc == kCols) {
+#pragma unroll
+                for (int q = 0; q < kCols / 4; ++q) {
+                    const float4 v = *reinterpret_cast<const float4*>(src + 4 * q);
+                    acc[4 * q] = fmaf(wp, v.x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(wp, v.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wp, v.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wp, v.w, acc[4 * q + 3]);
                 }
-            }
-        }
-    }
-    if (!active) return;
+            } else {
 #pragma unroll
-    for (int k = 0; k < kMaxCols; ++k) {
-        const int c = 2 * t + 256 * k;
-        if (c < d_c) st2(out + c, acc[k][0], acc[k][1]);
+                for (int e = 0; e < kCols; ++e)
+                    if (e < nc) acc[e] = fmaf(wp, src[e], acc[e]);
+            }
+        };
+#pragma unroll
+        for (int k = 0; k < kMergeRegs; ++k) {
+            if (32 * k >= np) break;
+            const int nj = (int)min((int64_t)32, np - 32 * k);
+            for (int j = 0; j < nj; ++j) add_piece(32 * k + j, __shfl_sync(0xffffffffu, lr[k], j));
+        }
+        for (int64_t p = 32 * kMergeRegs; p < np; ++p)
+            add_piece(p, part_l[piece_slot(first_w + p, seq0, per) * n_h + h]);
+#pragma unroll
+        for (int e = 0; e < kCols; e += 2)
+            if (e < nc) st2(out + c0 + e, acc[e], acc[e + 1]);
     }
 }
 
@@ -321,14 +330,13 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
                          const void* sched, const float* part_o, const float* part_l, void* o_lat,
                          float* lse, cudaStream_t s) {
-    if (d.d_c > 1024) return cudaErrorInvalidValue;
-    const dim3 grid(batch, (d.n_heads + 1) / 2);
+    const dim3 grid(batch, (d.n_heads + kMergeHeads - 1) / kMergeHeads);
     if (bf16)
-        merge_kernel<<<grid, 256, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                          (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
+        merge_kernel<<<grid, 32 * kMergeHeads, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                                       (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
     else
-        merge_kernel<<<grid, 256, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                          (float*)o_lat, lse, d.n_heads, d.d_c);
+        merge_kernel<<<grid, 32 * kMergeHeads, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
+                                                       (float*)o_lat, lse, d.n_heads, d.d_c);
     note_launch();
     return cudaGetLastError();
 }

@@ -198,6 +198,14 @@ __device__ __forceinline__ uint64_t kdesc64(uint32_t a) { return smem_desc(a, 16
 // MN-major 128B-swizzled B: 64-column atoms one TMA box (kTBox bytes) apart, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return smem_desc(a, kTBox, 1024, kSwizzle128B); }
 
+// 2^x with the special-function unit (relative error about 2^-22; the result is
+// rounded to bf16 right after, and exp2(-inf) = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
                 TcArgs a) {
@@ -369,19 +377,30 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 const float4 v = xr[c * kHeads];
                 s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
             }
-            // rows past the end of this piece do not count
+            // rows past the end of this piece do not count (only the last tile of a piece
+            // is partial)
             const int valid = co.valid_rows();
-            float mt = -INFINITY;
+            if (valid < kTok) {
 #pragma unroll
-            for (int j = 0; j < kTok; ++j) {
-                if (j >= valid) s[j] = -INFINITY;
-                mt = fmaxf(mt, s[j]);
+                for (int j = 0; j < kTok; ++j)
+                    if (j >= valid) s[j] = -INFINITY;
             }
+            // tile maximum: eight running maxima, then a tree (short dependency chains)
+            float m8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                m8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
+                              fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) m8[j] = fmaxf(m8[j], m8[j + w]);
+            const float mt = m8[0];
             // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
             const bool need = mt > m_run + 8.f;
             float alpha = 1.f;
             if (need) {
-                alpha = exp2f(m_run - mt);
+                alpha = fast_exp2(m_run - mt);
                 m_run = mt;
                 l_run *= alpha;
             }
@@ -402,13 +421,15 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             }
             // P tile (bf16) for the value MMA; the sum uses the rounded values
             uint32_t packed[kTok / 2];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};         // four partial sums (short chains)
 #pragma unroll
             for (int j = 0; j < kTok / 2; ++j) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(exp2f(s[2 * j] - m_run),
-                                                                exp2f(s[2 * j + 1] - m_run));
-                l_run += __low2float(h2) + __high2float(h2);
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_run),
+                                                                fast_exp2(s[2 * j + 1] - m_run));
+                ls[j & 3] += __low2float(h2) + __high2float(h2);
                 packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_st32u(tmem + lane_base + kColP, packed);
             if (valid < kTok) {
                 // the value MMA must not see rows of the tile beyond the piece (they may

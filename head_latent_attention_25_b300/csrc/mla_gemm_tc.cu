@@ -4,7 +4,8 @@
 //
 // The weights are the A operand (M = 128 output features per tile, TMA-loaded, K-major
 // or MN-major), the tokens are the B operand (N <= 128 per tile), the accumulator
-// lives in TMEM, and K is cut into 64-wide chunks streamed through a 4-stage ring.
+// lives in TMEM, and K is cut into 64-wide chunks streamed through a ring whose depth
+// is chosen per launch (all of a CTA's chunks in flight when shared memory allows).
 // For the cache append the long K (hidden = 7168) is also split across CTAs, which
 // write fp32 partial sums; a finalize kernel adds them in a fixed order, rotates the
 // k_R pairs and stores the bf16 cache rows.
@@ -24,18 +25,18 @@ using namespace tc;
 constexpr int kGM = 128;              // output features per tile (MMA M)
 constexpr int kGK = 64;               // K chunk (one 128-byte swizzle row of bf16)
 constexpr int kGNMax = 128;           // tokens per tile (MMA N)
-constexpr int kGStages = 4;
+constexpr int kGMaxStages = 8;        // ring depth is chosen per launch (stages <= this)
 constexpr int kGThreads = 128;
 constexpr uint32_t kATile = kGM * kGK * 2;      // 16 KB
 constexpr uint64_t kGTimeoutNs = 2000000000ull;
 
-// Shared memory per token-tile width: kGStages x (A tile + B tile) + barriers.
+// Shared memory per token-tile width: stages x (A tile + B tile), then barriers.
 template <int NT>
 struct GemmSmem {
     static constexpr uint32_t kBTile = NT * kGK * 2;
     static constexpr uint32_t kStage = kATile + kBTile;
-    static constexpr uint32_t kOffBar = kGStages * kStage;
-    static constexpr uint32_t kBytes = kOffBar + 128 + 1024;
+    static constexpr uint32_t kBarBytes = 256;
+    static uint32_t bytes(int stages) { return (uint32_t)stages * kStage + kBarBytes + 1024; }
 };
 
 enum GemmMode : int { kOutBf16 = 0, kOutPartial = 1 };
@@ -50,6 +51,7 @@ struct GemmTcArgs {
     int m_split_tile;     // M tiles >= this read the second weight map (rows - tile offset)
     int a2_rows;          // rows loaded from the second weight map (<= 128)
     int mode;
+    int stages;           // ring depth (1 .. kGMaxStages)
     float alpha;
     void* y; int64_t y_g, y_tok;      // bf16 output: y[g*y_g + t*y_tok + m]
     float* part; int part_ld;         // fp32 partial: part[(split*N + t)*part_ld + m]
@@ -92,10 +94,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t base = smem_addr(sm);
     using L = GemmSmem<NT>;
-    uint64_t* bars = (uint64_t*)(sm + L::kOffBar);
-    uint32_t* tslot = (uint32_t*)(sm + L::kOffBar + 96);
-    volatile int* abort_flag = (volatile int*)(sm + L::kOffBar + 100);
-    auto bar = [&](int i) { return smem_addr(&bars[i]); };   // 0..3 full, 4..7 empty, 8 done
+    const uint32_t off_bar = (uint32_t)a.stages * L::kStage;
+    uint64_t* bars = (uint64_t*)(sm + off_bar);
+    uint32_t* tslot = (uint32_t*)(sm + off_bar + 8 * (2 * kGMaxStages + 1));
+    volatile int* abort_flag = (volatile int*)(sm + off_bar + 8 * (2 * kGMaxStages + 1) + 4);
+    // barriers: [0, stages) full, [kGMaxStages, kGMaxStages + stages) empty, 2*kGMaxStages done
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    constexpr int E = kGMaxStages, DONE = 2 * kGMaxStages;
+    const uint32_t NS = (uint32_t)a.stages;
     constexpr uint32_t kBTile = L::kBTile;
     constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -107,8 +113,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     const uint32_t a_bytes = second ? (uint32_t)a.a2_rows * kGK * 2 : kATile;
 
     if (tid == 0) {
-        for (int i = 0; i < kGStages; ++i) { mbar_init(bar(i), 1); mbar_init(bar(4 + i), 1); }
-        mbar_init(bar(8), 1);
+        for (uint32_t i = 0; i < NS; ++i) { mbar_init(bar(i), 1); mbar_init(bar(E + i), 1); }
+        mbar_init(bar(DONE), 1);
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -125,8 +131,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         // producer
         uint32_t i = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++i) {
-            const uint32_t st = i % kGStages;
-            if (!gwait(bar(4 + st), ((i / kGStages) & 1) ^ 1, abort_flag, a.dev_status)) break;
+            const uint32_t st = i % NS;
+            if (!gwait(bar(E + st), ((i / NS) & 1) ^ 1, abort_flag, a.dev_status)) break;
             const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
             mbar_expect_tx(bar(st), a_bytes + kBTile);
             if (second) {
@@ -139,17 +145,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             }
             tma_load_3d(sb, &map_b, kc * kGK, g, n_tile * NT, bar(st));
         }
-        for (uint32_t k = 0; k < kGStages && k < i; ++k) {
+        for (uint32_t k = 0; k < NS && k < i; ++k) {
             const uint32_t j = i - 1 - k;
-            gdrain(bar(j % kGStages), (j / kGStages) & 1);
+            gdrain(bar(j % NS), (j / NS) & 1);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
         const uint32_t idesc = idesc_bf16_f32(kGM, NT, a.a_mn && !second ? 1u : 0u, 0u);
         uint32_t i = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++i) {
-            const uint32_t st = i % kGStages;
-            if (!gwait(bar(st), (i / kGStages) & 1, abort_flag, a.dev_status)) break;
+            const uint32_t st = i % NS;
+            if (!gwait(bar(st), (i / NS) & 1, abort_flag, a.dev_status)) break;
             tc_fence_after();
             const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
             for (int k = 0; k < kGK / 16; ++k) {
@@ -159,13 +165,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                 mma_bf16(tmem, da, smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B), idesc,
                          (i > 0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(bar(4 + st));
+            mma_commit(bar(E + st));
         }
-        mma_commit(bar(8));
+        mma_commit(bar(DONE));
     }
     // epilogue: thread <-> output feature (TMEM lane), 32 tokens per TMEM load
     __syncwarp();
-    const bool ok = gwait(bar(8), 0, abort_flag, a.dev_status);
+    const bool ok = gwait(bar(DONE), 0, abort_flag, a.dev_status);
     tc_fence_after();
     const int m = m_tile * kGM + warp * 32 + lane;
     const bool m_ok = m < a.M;
@@ -223,11 +229,18 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
     const float* p = part + (int64_t)t * width + e;
     const int64_t split_stride = (int64_t)n_tok * width;
     float v0 = 0.f, v1 = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < k_splits; ++s) {
-        const float2 x = *reinterpret_cast<const float2*>(p + s * split_stride);
-        v0 += x.x;
-        v1 += x.y;
+    constexpr int kBatch = 16;                  // loads in flight per thread
+    for (int s0 = 0; s0 < k_splits; s0 += kBatch) {
+        float2 x[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            x[q] = (s0 + q < k_splits) ? *reinterpret_cast<const float2*>(p + (s0 + q) * split_stride)
+                                       : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {      // split order, so the sum does not depend on timing
+            v0 += x[q].x;
+            v1 += x[q].y;
+        }
     }
     if (e >= d_c) {
         float c, sn;
@@ -277,14 +290,22 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtens
     const int m_tiles = (a.M + kGM - 1) / kGM;
     const int n_tiles = (a.N + nt - 1) / nt;
     dim3 grid(m_tiles, n_tiles, G * a.k_splits);
+    // ring depth: every K chunk of a CTA in flight at once when it fits, else as deep as
+    // shared memory allows
+    const uint32_t stage_bytes = kATile + (uint32_t)nt * kGK * 2;
+    int stages = min(a.chunks_per_split, kGMaxStages);
+    while (stages > 1 && (uint32_t)stages * stage_bytes + 256 + 1024 > 232448u) --stages;
+    a.stages = max(stages, 1);
     cudaError_t e;
 #define MLA_GEMM_CASE(NTV)                                                                         \
-    case NTV:                                                                                      \
+    case NTV: {                                                                                    \
+        const uint32_t smem = GemmSmem<NTV>::bytes(a.stages);                                       \
         e = cudaFuncSetAttribute(gemm_tc_kernel<NTV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)GemmSmem<NTV>::kBytes);                                      \
+                                 (int)smem);                                                      \
         if (e != cudaSuccess) return e;                                                           \
-        gemm_tc_kernel<NTV><<<grid, kGThreads, GemmSmem<NTV>::kBytes, s>>>(ma, ma2, mb, a);        \
-        break;
+        gemm_tc_kernel<NTV><<<grid, kGThreads, smem, s>>>(ma, ma2, mb, a);                         \
+        break;                                                                                    \
+    }
     switch (nt) {
         MLA_GEMM_CASE(16)
         MLA_GEMM_CASE(32)
@@ -300,6 +321,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtens
 GemmTcArgs gblank() {
     GemmTcArgs a{};
     a.k_splits = 1;
+    a.stages = 1;
     a.m_split_tile = 1 << 30;
     a.alpha = 1.f;
     a.mode = kOutBf16;
