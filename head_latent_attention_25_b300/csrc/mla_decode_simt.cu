@@ -240,8 +240,10 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
     // pass 2: lane owns columns [16 lane, 16 lane + 16) (+ 512 k for wider latents)
     constexpr int kCols = 16;
     const bool vec = (d_c % kCols) == 0;        // float4 loads stay aligned
-    for (int c0 = kCols * lane; c0 < d_c + 31 * kCols; c0 += 32 * kCols) {
+    const int rounds = (d_c + 32 * kCols - 1) / (32 * kCols);
+    for (int rd = 0; rd < rounds; ++rd) {
         // every lane runs the loop the same number of times (the shuffles need all 32)
+        const int c0 = kCols * lane + 32 * kCols * rd;
         float acc[kCols];
 #pragma unroll
         for (int e = 0; e < kCols; ++e) acc[e] = 0.f;

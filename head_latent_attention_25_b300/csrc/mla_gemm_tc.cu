@@ -30,13 +30,12 @@ constexpr int kGThreads = 128;
 constexpr uint32_t kATile = kGM * kGK * 2;      // 16 KB
 constexpr uint64_t kGTimeoutNs = 2000000000ull;
 
-// Shared memory per token-tile width: stages x (A tile + B tile), then barriers.
+// Shared memory per token-tile width: the ring of stages x (A tile + B tile), reused by
+// the epilogue as a staging tile, then the barriers (offset chosen per launch).
 template <int NT>
 struct GemmSmem {
     static constexpr uint32_t kBTile = NT * kGK * 2;
     static constexpr uint32_t kStage = kATile + kBTile;
-    static constexpr uint32_t kBarBytes = 256;
-    static uint32_t bytes(int stages) { return (uint32_t)stages * kStage + kBarBytes + 1024; }
 };
 
 enum GemmMode : int { kOutBf16 = 0, kOutPartial = 1 };
@@ -52,6 +51,8 @@ struct GemmTcArgs {
     int a2_rows;          // rows loaded from the second weight map (<= 128)
     int mode;
     int stages;           // ring depth (1 .. kGMaxStages)
+    int staged;           // bf16 output goes through a shared-memory tile (16-byte stores)
+    uint32_t off_bar;     // byte offset of the barriers: after the ring and the staging tile
     float alpha;
     void* y; int64_t y_g, y_tok;      // bf16 output: y[g*y_g + t*y_tok + m]
     float* part; int part_ld;         // fp32 partial: part[(split*N + t)*part_ld + m]
@@ -62,7 +63,7 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile in
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kGTimeoutNs) {
             *abort = 1;
@@ -94,7 +95,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t base = smem_addr(sm);
     using L = GemmSmem<NT>;
-    const uint32_t off_bar = (uint32_t)a.stages * L::kStage;
+    const uint32_t off_bar = a.off_bar;
     uint64_t* bars = (uint64_t*)(sm + off_bar);
     uint32_t* tslot = (uint32_t*)(sm + off_bar + 8 * (2 * kGMaxStages + 1));
     volatile int* abort_flag = (volatile int*)(sm + off_bar + 8 * (2 * kGMaxStages + 1) + 4);
@@ -175,13 +176,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     tc_fence_after();
     const int m = m_tile * kGM + warp * 32 + lane;
     const bool m_ok = m < a.M;
-    if (__all_sync(0xffffffffu, ok)) {
-        constexpr int kChunks = NT < 32 ? 1 : NT / 32;
-        constexpr int kCols = NT < 32 ? NT : 32;
+    const bool all_ok = __all_sync(0xffffffffu, ok);
+    constexpr int kChunks = NT < 32 ? 1 : NT / 32;
+    constexpr int kCols = NT < 32 ? NT : 32;
+    // bf16 output through shared memory: the stage ring is idle once the MMAs are done,
+    // and whole 128-feature rows (256 B) of a token go out as 16-byte stores
+    const bool staged = a.staged != 0;
+    constexpr int kLd = kGM + 4;                // fp32 row pitch of the staging tile
+    float* tile = reinterpret_cast<float*>(sm);
+    if (all_ok) {
         for (int c = 0; c < kChunks; ++c) {
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
             tmem_wait_ld();
+            if (staged) {
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) tile[(32 * c + j) * kLd + warp * 32 + lane] = a.alpha * v[j];
+                continue;
+            }
             if (!m_ok) continue;
             for (int j = 0; j < kCols; ++j) {
                 const int t = n_tile * NT + 32 * c + j;
@@ -194,6 +206,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             }
         }
     }
+    if (staged) {
+        __syncthreads();                        // every warp's columns are in the tile
+        if (all_ok) {
+            for (int e = tid; e < NT * (kGM / 8); e += kGThreads) {
+                const int j = e / (kGM / 8), f8 = e % (kGM / 8);
+                const int t = n_tile * NT + j;
+                if (t >= a.N) continue;
+                const float* src = tile + j * kLd + 8 * f8;
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
+                    w[q] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                *reinterpret_cast<uint4*>((__nv_bfloat16*)a.y + (int64_t)g * a.y_g + (int64_t)t * a.y_tok +
+                                          m_tile * kGM + 8 * f8) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
@@ -203,20 +234,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 }
 
 // cache row = [sum of partials for c ; RoPE(sum of partials for k_R, pos)] in bf16.
-// Grid (token, pair groups of kFinPairs): thread <-> one pair (2e, 2e+1) of one row,
-// which also keeps a rotary pair in one thread.  The split partials are added in
-// split order (fixed, so the result does not depend on timing); the loads of the
-// unrolled loop are independent, so several are in flight per thread.
-constexpr int kFinPairs = 128;
+// Grid (token, pair groups of kFinPairs): thread (x, y) of a block adds splits
+// y, y + kFinGroups, ... of pair x; the kFinGroups partial sums are then added in a
+// fixed order through shared memory (so the result does not depend on timing), and
+// the y = 0 threads rotate the k_R pairs and store the row.  A rotary pair stays in
+// one thread.
+constexpr int kFinPairs = 32;
+constexpr int kFinGroups = 8;
 
-__global__ void __launch_bounds__(kFinPairs)
+__global__ void __launch_bounds__(kFinPairs * kFinGroups)
 append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, int n_new, int d_c,
                        int d_r, double rope_r, const int64_t* __restrict__ row_off,
                        const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
                        int64_t cache_rows, __nv_bfloat16* __restrict__ cache, int32_t* dev_status) {
+    __shared__ float2 red[kFinGroups][kFinPairs];
     const int t = blockIdx.x;
     const int width = d_c + d_r;
-    const int e = 2 * (blockIdx.y * kFinPairs + threadIdx.x);
+    const int x = threadIdx.x % kFinPairs, y = threadIdx.x / kFinPairs;
+    const int e = 2 * (blockIdx.y * kFinPairs + x);
     const int b = t / n_new, j = t % n_new;
     const int p0 = pos0[b];
     const int64_t off = row_off[b], cp = cap[b];
@@ -224,24 +259,28 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
         if (j == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
         return;
     }
-    if (e >= width) return;
-    const int64_t pos = (int64_t)p0 + j;
-    const float* p = part + (int64_t)t * width + e;
-    const int64_t split_stride = (int64_t)n_tok * width;
-    float v0 = 0.f, v1 = 0.f;
-    constexpr int kBatch = 16;                  // loads in flight per thread
-    for (int s0 = 0; s0 < k_splits; s0 += kBatch) {
-        float2 x[kBatch];
+    float2 acc = make_float2(0.f, 0.f);
+    if (e < width) {
+        const float* p = part + (int64_t)t * width + e;
+        const int64_t split_stride = (int64_t)n_tok * width;
+        for (int s0 = y; s0 < k_splits; s0 += 4 * kFinGroups) {
+            float2 v[4];
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q)
-            x[q] = (s0 + q < k_splits) ? *reinterpret_cast<const float2*>(p + (s0 + q) * split_stride)
-                                       : make_float2(0.f, 0.f);
+            for (int q = 0; q < 4; ++q) {
+                const int sp = s0 + q * kFinGroups;
+                v[q] = sp < k_splits ? *reinterpret_cast<const float2*>(p + sp * split_stride) : make_float2(0.f, 0.f);
+            }
 #pragma unroll
-        for (int q = 0; q < kBatch; ++q) {      // split order, so the sum does not depend on timing
-            v0 += x[q].x;
-            v1 += x[q].y;
+            for (int q = 0; q < 4; ++q) { acc.x += v[q].x; acc.y += v[q].y; }
         }
     }
+    red[y][x] = acc;
+    __syncthreads();
+    if (y != 0 || e >= width) return;
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < kFinGroups; ++q) { v0 += red[q][x].x; v1 += red[q][x].y; }
+    const int64_t pos = (int64_t)p0 + j;
     if (e >= d_c) {
         float c, sn;
         rope_cos_sin(pos, (e - d_c) >> 1, rope_r, &c, &sn);
@@ -296,10 +335,16 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtens
     int stages = min(a.chunks_per_split, kGMaxStages);
     while (stages > 1 && (uint32_t)stages * stage_bytes + 256 + 1024 > 232448u) --stages;
     a.stages = max(stages, 1);
+    a.staged = a.mode == kOutBf16 && a.M % kGM == 0 && (a.y_tok % 8) == 0 && (a.y_g % 8) == 0 &&
+               ((uintptr_t)a.y % 16) == 0;
+    const uint32_t tile_bytes = (uint32_t)nt * (kGM + 4) * 4;
+    uint32_t ring = (uint32_t)a.stages * stage_bytes;
+    if (a.staged && tile_bytes > ring) ring = (tile_bytes + 1023) / 1024 * 1024;
+    a.off_bar = ring;
+    const uint32_t smem = ring + 256 + 1024;
     cudaError_t e;
 #define MLA_GEMM_CASE(NTV)                                                                         \
     case NTV: {                                                                                    \
-        const uint32_t smem = GemmSmem<NTV>::bytes(a.stages);                                       \
         e = cudaFuncSetAttribute(gemm_tc_kernel<NTV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)smem);                                                      \
         if (e != cudaSuccess) return e;                                                           \
@@ -380,7 +425,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
     cudaError_t e = run_gemm(ma, ma2, mb, a, 1, nt, s);
     if (e != cudaSuccess) return e;
     const dim3 fin_grid(n_tok, (width / 2 + kFinPairs - 1) / kFinPairs);
-    append_finalize_kernel<<<fin_grid, kFinPairs, 0, s>>>((const float*)workspace, splits, n_tok, n_new,
+    append_finalize_kernel<<<fin_grid, kFinPairs * kFinGroups, 0, s>>>((const float*)workspace, splits, n_tok, n_new,
                                                           d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
                                                           row_off, cap, pos0, cache_rows,
                                                           (__nv_bfloat16*)cache, dev_status);
