@@ -105,6 +105,8 @@ bool plan_decode(const mla_dims* d, mla_dtype t, int batch, int max_seq_len, int
     off = align_up(off + ws.cum_bytes, A);
     ws.sched_off = off; ws.sched_bytes = sizeof(Schedule);
     off = align_up(off + ws.sched_bytes, A);
+    ws.ws_off = off;    ws.ws_bytes = (size_t)w * sizeof(int32_t);
+    off = align_up(off + ws.ws_bytes, A);
     ws.po_off = off;    ws.po_bytes = (size_t)2 * w * d->n_heads * d->d_c * sizeof(float);
     off = align_up(off + ws.po_bytes, A);
     ws.pl_off = off;    ws.pl_bytes = (size_t)2 * w * d->n_heads * sizeof(float);
@@ -216,6 +218,7 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
     void* qp = ws + p.ws.q_off;
     int64_t* cum = (int64_t*)(ws + p.ws.cum_off);
     void* sched = ws + p.ws.sched_off;
+    int32_t* wstart = (int32_t*)(ws + p.ws.ws_off);
     float* part_o = (float*)(ws + p.ws.po_off);
     float* part_l = (float*)(ws + p.ws.pl_off);
     const bool bf16 = dtype == MLA_BF16;
@@ -228,14 +231,14 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
         e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
     }
     if (e == cudaSuccess)
-        e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, dev_status, s);
+        e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, wstart, dev_status, s);
     if (e == cudaSuccess) {
         if (tc)
             e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cache, cache_rows, row_off, cum,
-                                sched, o_lat, lse, part_o, part_l, dev_status, s);
+                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s);
         else
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
-                                  sched, o_lat, lse, part_o, part_l, s);
+                                  sched, wstart, o_lat, lse, part_o, part_l, s);
     }
     if (e == cudaSuccess)
         e = launch_merge(*dims, bf16, batch, cum, sched, part_o, part_l, o_lat, lse, s);

@@ -86,6 +86,7 @@ struct DecodeWorkspace {
     size_t q_off, q_bytes;          // folded query Q' [batch, n_h, d_c + d_r]
     size_t cum_off, cum_bytes;      // int64 prefix sums of sequence lengths [batch + 1]
     size_t sched_off, sched_bytes;  // Schedule
+    size_t ws_off, ws_bytes;        // int32 first sequence of each worker's range [workers]
     size_t po_off, po_bytes;        // partial o_lat [2*workers, n_h, d_c] fp32
     size_t pl_off, pl_bytes;        // partial log2-sum-exp [2*workers, n_h] fp32
     size_t total;

@@ -20,7 +20,8 @@ namespace {
 __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len,
                                                         const int64_t* row_off, int64_t cache_rows,
                                                         int batch, int workers, int64_t* cum,
-                                                        Schedule* sched, int32_t* dev_status) {
+                                                        Schedule* sched, int32_t* wstart,
+                                                        int32_t* dev_status) {
     __shared__ long long warp_tot[32];
     __shared__ long long carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -66,6 +67,19 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len,
         s.per = carry > 0 ? (carry + workers - 1) / workers : 1;
         *sched = s;
     }
+    __syncthreads();                            // cum complete and visible to the block
+    // first sequence of each worker's range: the last sequence whose rows start at or
+    // before the range start (saves every role of the split kernels a binary search)
+    const int64_t per = carry > 0 ? (carry + workers - 1) / workers : 1;
+    for (int g = tid; g < workers; g += 1024) {
+        const int64_t cur = (int64_t)g * per;
+        int lo = 0, hi = batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] <= cur) lo = mid; else hi = mid - 1;
+        }
+        wstart[g] = lo;
+    }
 }
 
 // ------------------------------------------------------------------ SIMT split
@@ -73,7 +87,7 @@ constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
 
 struct SplitArgs {
     const float* qp; const void* cache; const int64_t* row_off; const int64_t* cum;
-    const Schedule* sched; void* o_lat; float* lse; float* part_o; float* part_l;
+    const Schedule* sched; const int32_t* wstart; void* o_lat; float* lse; float* part_o; float* part_l;
     int n_h, d_c, d_r, batch;
 };
 
@@ -94,12 +108,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
     const bool active = h < a.n_h;
     const Tc* cache = (const Tc*)a.cache;
 
-    int lo = 0, hi = a.batch - 1;               // last sequence whose rows start at or before begin
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (a.cum[mid] <= begin) lo = mid; else hi = mid - 1;
-    }
-    int b = lo;
+    int b = a.wstart[g];                        // last sequence whose rows start at or before begin
     int64_t cur = begin;
     bool first = true;
     while (cur < end) {
@@ -283,10 +292,10 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
 }  // namespace
 
 cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
-                            int batch, int workers, int64_t* cum, void* sched, int32_t* dev_status,
-                            cudaStream_t s) {
+                            int batch, int workers, int64_t* cum, void* sched, int32_t* wstart,
+                            int32_t* dev_status, cudaStream_t s) {
     schedule_kernel<<<1, 1024, 0, s>>>(seq_len, row_off, cache_rows, batch, workers, cum,
-                                       (Schedule*)sched, dev_status);
+                                       (Schedule*)sched, wstart, dev_status);
     note_launch();
     return cudaGetLastError();
 }
@@ -303,9 +312,9 @@ int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count) {
 
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
-                              const void* sched, void* o_lat, float* lse, float* part_o,
-                              float* part_l, cudaStream_t s) {
-    SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, o_lat, lse, part_o, part_l,
+                              const void* sched, const int32_t* wstart, void* o_lat, float* lse,
+                              float* part_o, float* part_l, cudaStream_t s) {
+    SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, wstart, o_lat, lse, part_o, part_l,
                 d.n_heads, d.d_c, d.d_r, batch};
     const int dq = d.d_c + d.d_r;
     const size_t smem = (size_t)(kTileRows * (dq + 1) + kWarps * dq) * sizeof(float);

@@ -19,13 +19,16 @@
 // 100 KB of cache in flight.
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (the score MMA of tile T+1 is
-// issued before the value MMA of tile T), warp 2 TMEM owner, warps 4-7 softmax and
-// exchange (thread i <-> head i <-> TMEM lane i), warps 8-11 load Q' of each piece
-// into tensor memory and write each piece's output.  The exchange buffer is laid out
-// [16-byte chunk][head], so the 32 lanes of a warp write 512 contiguous bytes into
-// the peer (whole 32-byte sectors on the cluster interconnect); the peer's mbarrier
-// counts the bytes.  Every wait is bounded in time; on expiry the CTA raises
-// MLA_DEV_TIMEOUT, drains its own in-flight copies and MMAs, frees TMEM and returns.
+// issued before the value MMA of tile T), warp 2 TMEM owner, warp 3 returns exchange
+// credits to the peer, warps 4-7 and 8-11 two softmax/exchange groups that take
+// alternate tiles (thread i <-> head i <-> TMEM lane i), warps 12-15 load Q' of each
+// piece into tensor memory and write each piece's output.  Each group has its own
+// exchange buffer, laid out [16-byte chunk][head], so the 32 lanes of a warp write
+// 512 contiguous bytes into the peer (whole 32-byte sectors on the cluster
+// interconnect); the peer's mbarrier counts the bytes and a credit barrier returns
+// the buffer once the peer has read it.  Every
+// wait is bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains its own
+// in-flight copies and MMAs, frees TMEM and returns.
 #include <mutex>
 
 #include "mla_common.cuh"
@@ -41,7 +44,7 @@ using namespace tc;
 
 constexpr int kTok = 64;              // cache rows per tile (score MMA N, value MMA K)
 constexpr int kStages = 4;            // TMA ring depth
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kHeads = 128;           // MMA M (heads beyond n_heads are computed and dropped)
 constexpr int kLatHalf = 256;         // latent columns per CTA
 constexpr int kRopeHalf = 32;         // rotary columns per CTA
@@ -55,15 +58,17 @@ constexpr uint32_t kStageBytes = 4 * kTBox + kTRope;     // 36864
 constexpr uint32_t kXBytes = kHeads * kTok * 4;          // the peer's fp32 partial scores
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffStats = kOffX + 2 * kXBytes;      // [piece parity][m, l][head] fp32
-constexpr uint32_t kOffBar = kOffStats + 2 * 2 * kHeads * 4;
+constexpr uint32_t kOffStats = kOffX + 2 * kXBytes;      // [piece % 4][group][m, l][head] fp32
+constexpr uint32_t kOffMh = kOffStats + 4 * 2 * 2 * kHeads * 4;   // [tile parity][head] running max
+constexpr uint32_t kOffBar = kOffMh + 2 * kHeads * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers/flags + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier indices
 enum : int {
-    B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL, B_SEMPTY,
-    B_PFULL, B_VDONE, B_OFREE, B_XFULL, B_STATS = B_XFULL + 2, B_FIN, B_COUNT
+    B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
+    B_SEMPTY = B_SFULL + 2, B_PFULL, B_VDONE, B_OFREE = B_VDONE + 2, B_XFULL, B_XEMPTY = B_XFULL + 2,
+    B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS, B_COUNT = B_XCONS + 2
 };
 static_assert(B_COUNT * 8 <= 240, "barrier area");
 constexpr uint32_t kOffTslot = kOffBar + 240;
@@ -81,6 +86,7 @@ struct TcArgs {
     const int64_t* row_off;
     const int64_t* cum;
     const Schedule* sched;
+    const int32_t* wstart;             // first sequence of each worker's range
     __nv_bfloat16* o_lat;
     float* lse;
     float* part_o;
@@ -104,18 +110,14 @@ struct SegWalk {
     int64_t cur, end;
     int b, g;
     bool first;
-    __device__ void init(const int64_t* c, int batch, int gi, int64_t per, int64_t total) {
+    // start: the worker's first sequence, found by the schedule kernel
+    __device__ void init(const int64_t* c, int start, int gi, int64_t per, int64_t total) {
         cum = c;
         g = gi;
         cur = (int64_t)gi * per;
         end = min(cur + per, total);
         first = true;
-        int lo = 0, hi = batch - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (cum[mid] <= cur) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
+        b = start;
     }
     __device__ bool next(Seg& s) {
         if (cur >= end) return false;
@@ -231,13 +233,19 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
         mbar_init(bar(B_QFULL), 128);
         mbar_init(bar(B_QEMPTY), 1);
-        mbar_init(bar(B_SFULL), 1);
+        // score-ready and value-done barriers per tile parity: each phase of one is
+        // waited for in order by the group that owns (or follows) those tiles
+        for (int i = 0; i < 2; ++i) { mbar_init(bar(B_SFULL + i), 1); mbar_init(bar(B_VDONE + i), 1); }
         mbar_init(bar(B_SEMPTY), 128);
         mbar_init(bar(B_PFULL), 128);
-        mbar_init(bar(B_VDONE), 1);
         mbar_init(bar(B_OFREE), 128);
-        for (int i = 0; i < 2; ++i) mbar_init(bar(B_XFULL + i), 1);
-        mbar_init(bar(B_STATS), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_XFULL + i), 1);
+            mbar_init(bar(B_XEMPTY + i), 1);            // the peer's credit warp
+            mbar_init(bar(B_XCONS + i), 128);           // this CTA's group has read X[i]
+            mbar_init(bar(B_MH + i), 128);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_STATS + i), 256);
         mbar_init(bar(B_FIN), 1);
         *abort_flag = 0;
         fence_mbar_init_cluster();
@@ -255,11 +263,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
+    // Registers: 128 per thread at launch; each role re-sizes its warpgroup's share
+    // first thing in its own branch (80 + 168 + 168 + 96 = 4 x 128).
+    if (warp < 4) reg_alloc_dec<80>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             TileIt it;
-            it.walk.init(a.cum, a.batch, g, S.per, S.total);
+            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
             uint32_t issued = 0;
             while (it.next()) {
                 const uint32_t T = it.T, st = T % kStages;
@@ -284,8 +295,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
             const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
             TileIt sc, pv;                              // score-MMA and value-MMA positions
-            sc.walk.init(a.cum, a.batch, g, S.per, S.total);
-            pv.walk.init(a.cum, a.batch, g, S.per, S.total);
+            sc.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            pv.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
             bool ok = true;
             auto issue_score = [&]() -> bool {
                 const uint32_t T = sc.T, st = T % kStages;
@@ -300,7 +311,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                                 id_s, kk ? 1u : 0u);
                 for (int kk = 0; kk < 2; ++kk)
                     mma_bf16_ts(d, tmem + kColQ + 8 * (16 + kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
-                mma_commit(bar(B_SFULL));
+                mma_commit(bar(B_SFULL + (T & 1)));
                 if (sc.last_tile()) mma_commit(bar(B_QEMPTY));
                 return true;
             };
@@ -314,7 +325,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, mndesc128(stage + 2048 * k), id_o,
                                 (pv.first_tile() && k == 0) ? 0u : 1u);
                 mma_commit(bar(B_EMPTY + st));
-                mma_commit(bar(B_VDONE));
+                mma_commit(bar(B_VDONE + (T & 1)));
                 return true;
             };
             // Order: score(T+1) before value(T), so the next scores are computed while the
@@ -342,121 +353,161 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             mma_commit(bar(B_FIN));
             drain(bar(B_FIN), 0);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ softmax / exchange
-        const int i = tid - 128;                        // head row == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t peer_x = mapa(sX, peer);
-        const uint32_t peer_xfull = mapa(bar(B_XFULL), peer);
-        TileIt co;
-        co.walk.init(a.cum, a.batch, g, S.per, S.total);
-        bool ok = true;
-        float m_run = -INFINITY, l_run = 0.f;
-        while (ok && co.next()) {
-            const uint32_t T = co.T, xb = T & 1, st = T % kStages;
-            // this CTA's partial scores: out of TMEM, then to the peer
-            float s[kTok];
-            if (!(ok = wwait<false>(bar(B_SFULL), T & 1, ctl))) break;
-            tc_fence_after();
-            tmem_ld32(tmem + lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
-            tmem_ld32(tmem + lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(B_SEMPTY));
-            if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
-#pragma unroll
-            for (int c = 0; c < kTok / 4; ++c)
-                st_async_v4(peer_x + xb * kXBytes + (uint32_t)(c * kHeads + i) * 16, s[4 * c], s[4 * c + 1],
-                            s[4 * c + 2], s[4 * c + 3], peer_xfull + 8 * xb);
-            if (co.first_tile()) { m_run = -INFINITY; l_run = 0.f; }
-            // add the peer's partial scores of tile T
-            if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
-            const float4* xr = reinterpret_cast<const float4*>(sm + kOffX + xb * kXBytes) + i;
-#pragma unroll
-            for (int c = 0; c < kTok / 4; ++c) {
-                const float4 v = xr[c * kHeads];
-                s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
-            }
-            // rows past the end of this piece do not count (only the last tile of a piece
-            // is partial)
-            const int valid = co.valid_rows();
-            if (valid < kTok) {
-#pragma unroll
-                for (int j = 0; j < kTok; ++j)
-                    if (j >= valid) s[j] = -INFINITY;
-            }
-            // tile maximum: eight running maxima, then a tree (short dependency chains)
-            float m8[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                m8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
-                              fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
-#pragma unroll
-            for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                for (int j = 0; j < w; ++j) m8[j] = fmaxf(m8[j], m8[j + w]);
-            const float mt = m8[0];
-            // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
-            const bool need = mt > m_run + 8.f;
-            float alpha = 1.f;
-            if (need) {
-                alpha = fast_exp2(m_run - mt);
-                m_run = mt;
-                l_run *= alpha;
-            }
-            // the value MMA of the previous tile has finished with P and O
-            if (T > 0) {
-                if (!(ok = wwait<false>(bar(B_VDONE), (T - 1) & 1, ctl))) break;
-                tc_fence_after();
-            }
-            if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
-                for (int c = 0; c < kLatHalf / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= alpha;
-                    tmem_st32(tmem + lane_base + kColO + 32 * c, o);
-                }
-            }
-            // P tile (bf16) for the value MMA; the sum uses the rounded values
-            uint32_t packed[kTok / 2];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};         // four partial sums (short chains)
-#pragma unroll
-            for (int j = 0; j < kTok / 2; ++j) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_run),
-                                                                fast_exp2(s[2 * j + 1] - m_run));
-                ls[j & 3] += __low2float(h2) + __high2float(h2);
-                packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tmem_st32u(tmem + lane_base + kColP, packed);
-            if (valid < kTok) {
-                // the value MMA must not see rows of the tile beyond the piece (they may
-                // hold anything): zero them in this CTA's latent half of the stage
-                uint8_t* stage = sm + kOffStage + st * kStageBytes;
-                for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
-                    const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
-                    *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(B_PFULL));
-            if (co.last_tile()) {
-                float* sp = stats + (co.si & 1) * 2 * kHeads;
-                sp[i] = m_run;
-                sp[kHeads + i] = l_run;
-                mbar_arrive(bar(B_STATS));
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ exchange credits
+        // Returns each exchange buffer to the peer once the owning group has read it.
+        // The groups signal a local barrier (cheap); this warp, which has no remote
+        // stores of its own in flight, makes the cluster-scope release arrival.
+        if (lane == 0) {
+            TileIt it;
+            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            while (it.next()) {
+                const uint32_t T = it.T;
+                if (!wait<false>(bar(B_XCONS + (T & 1)), (T >> 1) & 1, ctl)) break;
+                mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ softmax / exchange
+        reg_alloc_inc<168>();
+        // Two groups of four warps take alternate tiles (group grp owns the tiles T with
+        // T % 2 == grp), so one group's exchange overlaps the other's exponentials.  The
+        // running maximum is handed from the owner of tile T-1 to the owner of tile T
+        // through shared memory; each group keeps its own sum relative to the maximum it
+        // last saw, and the epilogue combines the two.
+        const int grp = (warp - 4) >> 2;
+        const int i = (tid - 128) & (kHeads - 1);      // head row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t xb = (uint32_t)grp;              // this group's exchange buffer
+        const uint32_t peer_x = mapa(sX + xb * kXBytes, peer);
+        const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
+            float* mshare = (float*)(sm + kOffMh);
+        TileIt co;
+        co.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+        bool ok = true;
+        float m_g = -INFINITY, l_g = 0.f;
+        while (ok && co.next()) {
+            const uint32_t T = co.T;
+            if (co.first_tile()) { m_g = -INFINITY; l_g = 0.f; }
+            if ((T & 1u) == xb) {
+                const uint32_t st = T % kStages;
+                // this CTA's partial scores: out of TMEM, then to the peer
+                float s[kTok];
+                if (!(ok = wwait<false>(bar(B_SFULL + xb), (T >> 1) & 1, ctl))) break;
+                tc_fence_after();
+                tmem_ld32(tmem + lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
+                tmem_ld32(tmem + lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(B_SEMPTY));
+                // the peer has finished reading what this group sent for tile T - 2
+                if (T >= 2 && !(ok = wwait<true>(bar(B_XEMPTY + xb), ((T >> 1) - 1) & 1, ctl))) break;
+                if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
+#pragma unroll
+                for (int c = 0; c < kTok / 4; ++c)
+                    st_async_v4(peer_x + (uint32_t)(c * kHeads + i) * 16, s[4 * c], s[4 * c + 1],
+                                s[4 * c + 2], s[4 * c + 3], peer_xfull);
+                // add the peer's partial scores of tile T
+                if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
+                const float4* xr = reinterpret_cast<const float4*>(sm + kOffX + xb * kXBytes) + i;
+#pragma unroll
+                for (int c = 0; c < kTok / 4; ++c) {
+                    const float4 v = xr[c * kHeads];
+                    s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
+                }
+                mbar_arrive(bar(B_XCONS + xb));
+                // rows past the end of this piece do not count (only the last tile of a
+                // piece is partial)
+                const int valid = co.valid_rows();
+                if (valid < kTok) {
+#pragma unroll
+                    for (int j = 0; j < kTok; ++j)
+                        if (j >= valid) s[j] = -INFINITY;
+                }
+                // tile maximum: eight running maxima, then a tree (short dependency chains)
+                float m8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    m8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
+                                  fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
+#pragma unroll
+                for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) m8[j] = fmaxf(m8[j], m8[j + w]);
+                const float mt = m8[0];
+                // the running maximum after tile T - 1 (decided by the other group)
+                if (T > 0) {
+                    if (!(ok = wwait<false>(bar(B_MH + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                    const float mp = mshare[((T - 1) & 1) * kHeads + i];
+                    if (!co.first_tile() && mp != m_g) { l_g *= fast_exp2(m_g - mp); m_g = mp; }
+                }
+                // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
+                const bool need = mt > m_g + 8.f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = fast_exp2(m_g - mt);
+                    m_g = mt;
+                    l_g *= alpha;
+                }
+                mshare[(T & 1) * kHeads + i] = m_g;
+                mbar_arrive(bar(B_MH + (T & 1)));
+                // the value MMA of the previous tile has finished with P and O
+                if (T > 0) {
+                    if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                    tc_fence_after();
+                }
+                if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
+                    for (int c = 0; c < kLatHalf / 16; ++c) {
+                        float o[16];
+                        tmem_ld16(tmem + lane_base + kColO + 16 * c, o);
+                        tmem_wait_ld();
+                        uint32_t u[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(o[j] * alpha);
+                        tmem_st16(tmem + lane_base + kColO + 16 * c, u);
+                    }
+                }
+                // P tile (bf16) for the value MMA; the sum uses the rounded values
+                uint32_t packed[kTok / 2];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums (short chains)
+#pragma unroll
+                for (int j = 0; j < kTok / 2; ++j) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_g),
+                                                                    fast_exp2(s[2 * j + 1] - m_g));
+                    ls[j & 3] += __low2float(h2) + __high2float(h2);
+                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tmem_st32u(tmem + lane_base + kColP, packed);
+                if (valid < kTok) {
+                    // the value MMA must not see rows of the tile beyond the piece (they may
+                    // hold anything): zero them in this CTA's latent half of the stage
+                    uint8_t* stage = sm + kOffStage + st * kStageBytes;
+                    for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
+                        const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
+                        *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(B_PFULL));
+            }
+            if (co.last_tile()) {
+                // this group's share of the piece's statistics
+                float* sp = stats + ((co.si & 3) * 2 + grp) * 2 * kHeads;
+                sp[i] = m_g;
+                sp[kHeads + i] = l_g;
+                mbar_arrive(bar(B_STATS + (co.si & 3)));
+            }
+        }
+    } else if (warp >= 12) {
         // ------------------------------------------------------------ Q' loader / epilogue
-        const int i = tid - 256;                        // head row == TMEM lane
+        reg_alloc_dec<96>();
+        const int i = tid - 384;                        // head row == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         SegWalk walk;
-        walk.init(a.cum, a.batch, g, S.per, S.total);
+        walk.init(a.cum, a.wstart[g], g, S.per, S.total);
         Seg cur, nxt;
         bool have = walk.next(cur);
         uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
@@ -465,32 +516,24 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const bool row_ok = i < a.n_h;
             const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            {   // latent columns [256r, 256r + 128)
-                uint32_t r[2][32];
+            // latent columns [256r, 256r + 256) in four chunks of 64 bf16 (32 TMEM columns)
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                uint32_t r[32];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 v = row_ok ? src[rank * 32 + c] : zero;
-                    r[c >> 3][4 * (c & 7)] = v.x; r[c >> 3][4 * (c & 7) + 1] = v.y;
-                    r[c >> 3][4 * (c & 7) + 2] = v.z; r[c >> 3][4 * (c & 7) + 3] = v.w;
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = row_ok ? src[rank * 32 + 8 * k + c] : zero;
+                    r[4 * c] = v.x; r[4 * c + 1] = v.y; r[4 * c + 2] = v.z; r[4 * c + 3] = v.w;
                 }
-                tmem_st32u(tmem + lane_base + kColQ, r[0]);
-                tmem_st32u(tmem + lane_base + kColQ + 32, r[1]);
+                tmem_st32u(tmem + lane_base + kColQ + 32 * k, r);
             }
-            {   // latent columns [256r + 128, 256r + 256) and rotary [512 + 32r, +32)
-                uint32_t r[2][32], q[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 v = row_ok ? src[rank * 32 + 16 + c] : zero;
-                    r[c >> 3][4 * (c & 7)] = v.x; r[c >> 3][4 * (c & 7) + 1] = v.y;
-                    r[c >> 3][4 * (c & 7) + 2] = v.z; r[c >> 3][4 * (c & 7) + 3] = v.w;
-                }
+            {   // rotary columns [512 + 32r, 512 + 32r + 32)
+                uint32_t q[16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v = row_ok ? src[64 + rank * 4 + c] : zero;
                     q[4 * c] = v.x; q[4 * c + 1] = v.y; q[4 * c + 2] = v.z; q[4 * c + 3] = v.w;
                 }
-                tmem_st32u(tmem + lane_base + kColQ + 64, r[0]);
-                tmem_st32u(tmem + lane_base + kColQ + 96, r[1]);
                 tmem_st16(tmem + lane_base + kColQ + 128, q);
             }
             tmem_wait_st();
@@ -509,10 +552,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 load_q(nxt);
             }
             // epilogue of this piece: O_r / l, log2-sum-exp
-            if (!(ok = wwait<false>(bar(B_STATS), si & 1, ctl))) break;
-            const float* sp = stats + (si & 1) * 2 * kHeads;
-            const float m_fin = sp[i], l_fin = sp[kHeads + i];
-            if (!(ok = wwait<false>(bar(B_VDONE), (t_end - 1) & 1, ctl))) break;
+            if (!(ok = wwait<false>(bar(B_STATS + (si & 3)), (si >> 2) & 1, ctl))) break;
+            const float* sp = stats + (si & 3) * 4 * kHeads;
+            const float m0 = sp[i], l0 = sp[kHeads + i], m1 = sp[2 * kHeads + i], l1 = sp[3 * kHeads + i];
+            const float m_fin = fmaxf(m0, m1);
+            const float l_fin = l0 * exp2f(m0 - m_fin) + l1 * exp2f(m1 - m_fin);
+            if (!(ok = wwait<false>(bar(B_VDONE + ((t_end - 1) & 1)), ((t_end - 1) >> 1) & 1, ctl))) break;
             tc_fence_after();
             const float inv = 1.f / l_fin;
             const float lse2 = m_fin + log2f(l_fin);
@@ -593,7 +638,7 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, ui
 
 int tc_workers(int64_t max_total_rows, int sm_count) {
     int64_t w = sm_count / 2;                           // one 2-CTA cluster per SM pair
-    const int64_t by_rows = (max_total_rows + 4 * kTok - 1) / (4 * kTok);
+    const int64_t by_rows = (max_total_rows + kTok - 1) / kTok;
     if (w > by_rows) w = by_rows;
     if (w < 1) w = 1;
     return (int)w;
@@ -602,16 +647,16 @@ int tc_workers(int64_t max_total_rows, int sm_count) {
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
                             int64_t q_rows, const void* cache, int64_t cache_rows,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
-                            void* o_lat, float* lse, float* part_o, float* part_l,
-                            int32_t* dev_status, cudaStream_t s) {
+                            const int32_t* wstart, void* o_lat, float* lse, float* part_o,
+                            float* part_l, int32_t* dev_status, cudaStream_t s) {
     (void)q_rows;
     if (!get_encoder()) return cudaErrorNotSupported;
     CUtensorMap mc128, mc64;
     if (!encode_2d(&mc128, cache, kRowElems, (uint64_t)cache_rows, 64, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    TcArgs a{(const __nv_bfloat16*)qp, row_off, cum, (const Schedule*)sched, (__nv_bfloat16*)o_lat, lse,
-             part_o, part_l, dev_status, d.n_heads, batch};
+    TcArgs a{(const __nv_bfloat16*)qp, row_off, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
+             lse, part_o, part_l, dev_status, d.n_heads, batch};
     cudaError_t e = cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -46,21 +46,21 @@ cudaError_t launch_project_out_tc(const mla_dims& d, int batch, const void* o_la
 // Work split of the flattened context: prefix sums of the usable sequence lengths and
 // the Schedule, written into the workspace; flags unusable sequences.
 cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
-                            int batch, int workers, int64_t* cum, void* sched, int32_t* dev_status,
-                            cudaStream_t s);
+                            int batch, int workers, int64_t* cum, void* sched, int32_t* wstart,
+                            int32_t* dev_status, cudaStream_t s);
 
 // fp32-Q' SIMT split kernel (any supported dims, fp32 or bf16 cache).
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
-                              const void* sched, void* o_lat, float* lse, float* part_o,
-                              float* part_l, cudaStream_t s);
+                              const void* sched, const int32_t* wstart, void* o_lat, float* lse,
+                              float* part_o, float* part_l, cudaStream_t s);
 
 // bf16 tcgen05 split kernel for d_c = 512, d_r = 64, n_heads <= 128 (2-CTA clusters).
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
                             int64_t q_rows, const void* cache, int64_t cache_rows,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
-                            void* o_lat, float* lse, float* part_o, float* part_l,
-                            int32_t* dev_status, cudaStream_t s);
+                            const int32_t* wstart, void* o_lat, float* lse, float* part_o,
+                            float* part_l, int32_t* dev_status, cudaStream_t s);
 
 // Combines the partial results of sequences cut across workers; zero-fills empty ones.
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,

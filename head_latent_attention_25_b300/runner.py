@@ -120,6 +120,24 @@ class DecodeStep:
         self.decode(stream)
         self.project_out(stream)
 
+    def capture(self, stream: Optional[torch.cuda.Stream] = None) -> torch.cuda.CUDAGraph:
+        """Record ``step`` once into a CUDA graph; ``graph.replay()`` re-runs the whole path.
+
+        Every call of the path is asynchronous, allocation-free and synchronisation-free,
+        so it can be captured; the buffers (and the workspace) are the ones bound here,
+        and the device-side index arrays may change between replays.
+        """
+        g = torch.cuda.CUDAGraph()
+        s = stream if stream is not None else torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step(s)                       # warm-up outside capture (lazy loads, attributes)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            self.step(s)
+        return g
+
     def new_rows(self, b: int) -> torch.Tensor:
         o = int(self.row_off[b].item()) + self.ctx_lens[b]
         return self.cache[o:o + self.n_new]
