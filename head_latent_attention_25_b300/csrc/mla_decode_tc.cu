@@ -35,6 +35,7 @@
 #include "mla_internal.h"
 #include "tc_ptx.cuh"
 
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 namespace mla {
@@ -55,13 +56,17 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr uint32_t kTBox = kTok * 128;                   // 64 rows x 64 bf16, 128B swizzle
 constexpr uint32_t kTRope = kTok * 64;                   // 64 rows x 32 bf16, 64B swizzle
 constexpr uint32_t kStageBytes = 4 * kTBox + kTRope;     // 36864
-constexpr uint32_t kXBytes = kHeads * kTok * 4;          // the peer's fp32 partial scores
+// the peer's partial scores of one tile: per head an fp32 offset (the partial of the
+// tile's first row) and 64 fp16 differences from it
+constexpr uint32_t kXResBytes = kHeads * kTok * 2;
+constexpr uint32_t kXBytes = kXResBytes + kHeads * 4;
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kOffStats = kOffX + 2 * kXBytes;      // [piece % 4][group][m, l][head] fp32
 constexpr uint32_t kOffMh = kOffStats + 4 * 2 * 2 * kHeads * 4;   // [tile parity][head] running max
 constexpr uint32_t kOffBar = kOffMh + 2 * kHeads * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;   // barriers/flags + alignment slack
+constexpr uint32_t kBarBytes = 320;                      // mbarriers, then the TMEM slot and abort flag
+constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier indices
@@ -70,9 +75,9 @@ enum : int {
     B_SEMPTY = B_SFULL + 2, B_PFULL, B_VDONE, B_OFREE = B_VDONE + 2, B_XFULL, B_XEMPTY = B_XFULL + 2,
     B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS, B_COUNT = B_XCONS + 2
 };
-static_assert(B_COUNT * 8 <= 240, "barrier area");
-constexpr uint32_t kOffTslot = kOffBar + 240;
-constexpr uint32_t kOffAbort = kOffBar + 244;
+static_assert(B_COUNT * 8 <= kBarBytes, "barrier area");
+constexpr uint32_t kOffTslot = kOffBar + kBarBytes;
+constexpr uint32_t kOffAbort = kOffTslot + 4;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -403,17 +408,41 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 // the peer has finished reading what this group sent for tile T - 2
                 if (T >= 2 && !(ok = wwait<true>(bar(B_XEMPTY + xb), ((T >> 1) - 1) & 1, ctl))) break;
                 if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
+                {
+                    // block-scaled fp16: s = off + r with off the partial of the tile's first
+                    // row (always a row of the piece), so each r is rounded relative to the
+                    // spread of the partial within the tile, not to its magnitude
+                    // (|error| <= 2^-11 |s - off|)
+                    const float off = s[0];
 #pragma unroll
-                for (int c = 0; c < kTok / 4; ++c)
-                    st_async_v4(peer_x + (uint32_t)(c * kHeads + i) * 16, s[4 * c], s[4 * c + 1],
-                                s[4 * c + 2], s[4 * c + 3], peer_xfull);
+                    for (int c = 0; c < kTok / 8; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 h2 = __floats2half2_rn(s[8 * c + 2 * e] - off, s[8 * c + 2 * e + 1] - off);
+                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        st_async_v4u(peer_x + (uint32_t)(c * kHeads + i) * 16, w[0], w[1], w[2], w[3], peer_xfull);
+                    }
+                    st_async_f32(peer_x + kXResBytes + (uint32_t)i * 4, off, peer_xfull);
+                }
                 // add the peer's partial scores of tile T
                 if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
-                const float4* xr = reinterpret_cast<const float4*>(sm + kOffX + xb * kXBytes) + i;
+                {
+                    const uint8_t* xbase = sm + kOffX + xb * kXBytes;
+                    const uint4* xr = reinterpret_cast<const uint4*>(xbase) + i;
+                    const float off = reinterpret_cast<const float*>(xbase + kXResBytes)[i];
 #pragma unroll
-                for (int c = 0; c < kTok / 4; ++c) {
-                    const float4 v = xr[c * kHeads];
-                    s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
+                    for (int c = 0; c < kTok / 8; ++c) {
+                        const uint4 v = xr[c * kHeads];
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                            s[8 * c + 2 * e] += f.x + off;
+                            s[8 * c + 2 * e + 1] += f.y + off;
+                        }
+                    }
                 }
                 mbar_arrive(bar(B_XCONS + xb));
                 // rows past the end of this piece do not count (only the last tile of a
