@@ -18,9 +18,8 @@
 // 4-stage ring of cache tiles and two exchange buffers, so each CTA keeps about
 // 100 KB of cache in flight.
 //
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (the score MMA of tile T+1 is
-// issued before the value MMA of tile T), warp 2 TMEM owner, warp 3 returns exchange
-// credits to the peer, warps 4-7 and 8-11 two softmax/exchange groups that take
+// Warp roles: warp 0 TMA producer, warp 1 issues the score MMAs, warp 2 owns the
+// tensor memory and issues the value MMAs, warp 3 returns exchange credits to the peer, warps 4-7 and 8-11 two softmax/exchange groups that take
 // alternate tiles (thread i <-> head i <-> TMEM lane i), warps 12-15 load Q' of each
 // piece into tensor memory and write each piece's output.  Each group has its own
 // exchange buffer, laid out [16-byte chunk][head], so the 32 lanes of a warp write
@@ -251,7 +250,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             mbar_init(bar(B_MH + i), 128);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_STATS + i), 256);
-        mbar_init(bar(B_FIN), 1);
+        mbar_init(bar(B_FIN), 2);                     // one commit per MMA issuer
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -294,67 +293,51 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Warp 1 issues the score MMAs, warp 2 the value MMAs: two independent issue
+        // streams, so the score of tile T+1 never waits behind the value MMA of tile T
+        // (which waits for tile T's softmax).  The two touch disjoint tensor memory
+        // (S; O, P, Q'); a stage is released by the value MMA, which always completes
+        // after the score MMA of the same tile (the softmax in between needs it).
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
-            const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
-            TileIt sc, pv;                              // score-MMA and value-MMA positions
-            sc.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-            pv.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            TileIt it;
+            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
             bool ok = true;
-            auto issue_score = [&]() -> bool {
-                const uint32_t T = sc.T, st = T % kStages;
-                if (sc.first_tile() && !wait<false>(bar(B_QFULL), sc.si & 1, ctl)) return false;
-                if (!wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl)) return false;
-                if (T > 0 && !wait<false>(bar(B_SEMPTY), (T - 1) & 1, ctl)) return false;
-                tc_fence_after();
-                const uint32_t stage = sStage + st * kStageBytes;
-                const uint32_t d = tmem + kColS;
-                for (int kk = 0; kk < 16; ++kk)
-                    mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
-                                id_s, kk ? 1u : 0u);
-                for (int kk = 0; kk < 2; ++kk)
-                    mma_bf16_ts(d, tmem + kColQ + 8 * (16 + kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
-                mma_commit(bar(B_SFULL + (T & 1)));
-                if (sc.last_tile()) mma_commit(bar(B_QEMPTY));
-                return true;
-            };
-            auto issue_value = [&]() -> bool {
-                const uint32_t T = pv.T, st = T % kStages;
-                if (!wait<false>(bar(B_PFULL), T & 1, ctl)) return false;
-                if (pv.first_tile() && pv.si > 0 && !wait<false>(bar(B_OFREE), (pv.si - 1) & 1, ctl)) return false;
-                tc_fence_after();
-                const uint32_t stage = sStage + st * kStageBytes;
-                for (int k = 0; k < kTok / 16; ++k)
-                    mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, mndesc128(stage + 2048 * k), id_o,
-                                (pv.first_tile() && k == 0) ? 0u : 1u);
-                mma_commit(bar(B_EMPTY + st));
-                mma_commit(bar(B_VDONE + (T & 1)));
-                return true;
-            };
-            // Order: score(T+1) before value(T), so the next scores are computed while the
-            // softmax of tile T runs -- except when tile T+1 opens a new piece: its score
-            // MMA waits for that piece's Q', and value(T) (which the piece's epilogue
-            // waits for) must not queue behind that load.
-            bool more = sc.next();
-            if (more) {
-                ok = issue_score();
-                more = sc.next();
-            }
-            while (ok && pv.next()) {
-                const bool early = more && !sc.first_tile();
-                if (early) {
-                    ok = issue_score();
-                    more = sc.next();
-                    if (!ok) break;
+            if (warp == 1) {
+                const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
+                while (ok && it.next()) {
+                    const uint32_t T = it.T, st = T % kStages;
+                    if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
+                    if (!(ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl))) break;
+                    if (T > 0 && !(ok = wait<false>(bar(B_SEMPTY), (T - 1) & 1, ctl))) break;
+                    tc_fence_after();
+                    const uint32_t stage = sStage + st * kStageBytes;
+                    const uint32_t d = tmem + kColS;
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
+                                    id_s, kk ? 1u : 0u);
+                    for (int kk = 0; kk < 2; ++kk)
+                        mma_bf16_ts(d, tmem + kColQ + 8 * (16 + kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
+                    mma_commit(bar(B_SFULL + (T & 1)));
+                    if (it.last_tile()) mma_commit(bar(B_QEMPTY));
                 }
-                ok = issue_value();
-                if (ok && more && !early) {
-                    ok = issue_score();
-                    more = sc.next();
+            } else {
+                const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
+                while (ok && it.next()) {
+                    const uint32_t T = it.T, st = T % kStages;
+                    if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
+                    if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
+                    tc_fence_after();
+                    const uint32_t stage = sStage + st * kStageBytes;
+                    for (int k = 0; k < kTok / 16; ++k)
+                        mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, mndesc128(stage + 2048 * k), id_o,
+                                    (it.first_tile() && k == 0) ? 0u : 1u);
+                    mma_commit(bar(B_EMPTY + st));
+                    mma_commit(bar(B_VDONE + (T & 1)));
                 }
             }
+            // every MMA this thread issued has completed before the CTA may tear down
             mma_commit(bar(B_FIN));
             drain(bar(B_FIN), 0);
         }
@@ -665,8 +648,35 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, ui
 
 }  // namespace
 
+// How many 2-CTA clusters of the attention kernel can be resident at once on the
+// current device (a cluster must sit inside one GPC, so this can be below sm_count/2);
+// 0 when the query is not available.
+int resident_pairs() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+            cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * 256);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = kSmemBytes;
+            if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel, &cfg) != cudaSuccess) n = 0;
+        }
+        (void)cudaGetLastError();
+        cache[dev] = n > 0 ? n : -1;
+    }
+    return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 int tc_workers(int64_t max_total_rows, int sm_count) {
     int64_t w = sm_count / 2;                           // one 2-CTA cluster per SM pair
+    const int resident = resident_pairs();              // all workers in one wave
+    if (resident > 0 && w > resident) w = resident;
     const int64_t by_rows = (max_total_rows + kTok - 1) / kTok;
     if (w > by_rows) w = by_rows;
     if (w < 1) w = 1;
