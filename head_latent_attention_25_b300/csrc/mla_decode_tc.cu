@@ -6,28 +6,30 @@
 // [256r, 256r+256) and rotary columns [512+32r, 512+32r+32) of every cache row, so
 // the pair streams each row from HBM exactly once.  Per tile of 64 rows:
 //
-//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=64 rows, K=288; Q'_r is the A
-//                            operand in tensor memory, the cache tile the B operand
-//   S   = S_0 + S_1          each CTA sends its fp32 partial to the peer (DSMEM)
+//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=64 rows, K=288; the latent part
+//                            of Q'_r is the A operand in tensor memory, its rotary
+//                            part in shared memory; the cache tile is the B operand
+//   S   = S_0 + S_1          each CTA sends its partial to the peer (DSMEM), as an
+//                            fp32 offset per head plus fp16 differences
 //   P   = exp2(S - m)        online softmax (identical in both CTAs; lazy max update)
-//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=64; P (bf16) in tensor memory,
+//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=64; P (bf16) from shared memory,
 //                            the cache tile read again as an MN-major B operand
 //
-// Tensor memory (512 columns): O_r 128 x 256 fp32, Q'_r 128 x 288 bf16 (144 columns),
-// S 128 x 64 fp32, P 128 x 64 bf16 (32 columns).  Shared memory holds only the
-// 4-stage ring of cache tiles and two exchange buffers, so each CTA keeps about
-// 100 KB of cache in flight.
+// Tensor memory (512 columns): O_r 128 x 256 fp32, the latent part of Q'_r 128 x 256
+// bf16 (128 columns), S[2] 2 x 128 x 64 fp32 (one per tile parity).  Shared memory:
+// a 4-stage ring of cache tiles (about 147 KB in flight), two exchange buffers, P and
+// the rotary part of Q'_r.
 //
-// Warp roles: warp 0 TMA producer, warp 1 issues the score MMAs, warp 2 owns the
-// tensor memory and issues the value MMAs, warp 3 returns exchange credits to the peer, warps 4-7 and 8-11 two softmax/exchange groups that take
-// alternate tiles (thread i <-> head i <-> TMEM lane i), warps 12-15 load Q' of each
-// piece into tensor memory and write each piece's output.  Each group has its own
-// exchange buffer, laid out [16-byte chunk][head], so the 32 lanes of a warp write
-// 512 contiguous bytes into the peer (whole 32-byte sectors on the cluster
-// interconnect); the peer's mbarrier counts the bytes and a credit barrier returns
-// the buffer once the peer has read it.  Every
-// wait is bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains its own
-// in-flight copies and MMAs, frees TMEM and returns.
+// Warp roles: warp 0 TMA producer and exchange credits, warps 1 and 3 issue the score
+// MMAs of the even and odd tiles, warp 2 owns the tensor memory and issues the value
+// MMAs, warps 4-7 and 8-11 two softmax/exchange groups that take alternate tiles
+// (thread i <-> head i <-> TMEM lane i), warps 12-15 load Q' of each piece and write
+// each piece's output.  Each group has its own exchange buffer, laid out [16-byte
+// chunk][head], so the 32 lanes of a warp write 512 contiguous bytes into the peer
+// (whole 32-byte sectors on the cluster interconnect); the peer's mbarrier counts the
+// bytes and a credit returns the buffer once the peer has read it.  Every wait is
+// bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains its own in-flight
+// copies and MMAs, frees TMEM and returns.
 #include <mutex>
 
 #include "mla_common.cuh"
@@ -61,18 +63,22 @@ constexpr uint32_t kXResBytes = kHeads * kTok * 2;
 constexpr uint32_t kXBytes = kXResBytes + kHeads * 4;
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffStats = kOffX + 2 * kXBytes;      // [piece % 4][group][m, l][head] fp32
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;          // P: 128 heads x 64 rows bf16, K-major, 128B swizzle
+constexpr uint32_t kOffQR = kOffP + kHeads * 128;         // rotary part of Q'_r: 128 x 32 bf16, 64B swizzle
+constexpr uint32_t kOffStats = kOffQR + kHeads * 64;      // [piece % 4][group][m, l][head] fp32
 constexpr uint32_t kOffMh = kOffStats + 4 * 2 * 2 * kHeads * 4;   // [tile parity][head] running max
 constexpr uint32_t kOffBar = kOffMh + 2 * kHeads * 4;
 constexpr uint32_t kBarBytes = 320;                      // mbarriers, then the TMEM slot and abort flag
 constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffP % 1024 == 0 && kOffQR % 1024 == 0, "swizzled operands need 1024-byte alignment");
 
 // barrier indices
 enum : int {
     B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
-    B_SEMPTY = B_SFULL + 2, B_PFULL, B_VDONE, B_OFREE = B_VDONE + 2, B_XFULL, B_XEMPTY = B_XFULL + 2,
-    B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS, B_COUNT = B_XCONS + 2
+    B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_VDONE, B_OFREE = B_VDONE + 2, B_XFULL,
+    B_XEMPTY = B_XFULL + 2, B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS,
+    B_COUNT = B_XCONS + 2
 };
 static_assert(B_COUNT * 8 <= kBarBytes, "barrier area");
 constexpr uint32_t kOffTslot = kOffBar + kBarBytes;
@@ -81,9 +87,8 @@ constexpr uint32_t kOffAbort = kOffTslot + 4;
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;          // O_r: 256 fp32 columns
-constexpr uint32_t kColQ = 256;        // Q'_r: 288 bf16 = 144 columns
-constexpr uint32_t kColS = 416;        // S: 64 fp32 columns
-constexpr uint32_t kColP = 480;        // P: 64 bf16 = 32 columns
+constexpr uint32_t kColQ = 256;        // latent part of Q'_r: 256 bf16 = 128 columns
+constexpr uint32_t kColS = 384;        // S[2] (by tile parity): 2 x 64 fp32 columns
 
 struct TcArgs {
     const __nv_bfloat16* qp;           // folded queries [batch * n_h, 576]
@@ -236,11 +241,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
         mbar_init(bar(B_QFULL), 128);
-        mbar_init(bar(B_QEMPTY), 1);
-        // score-ready and value-done barriers per tile parity: each phase of one is
-        // waited for in order by the group that owns (or follows) those tiles
-        for (int i = 0; i < 2; ++i) { mbar_init(bar(B_SFULL + i), 1); mbar_init(bar(B_VDONE + i), 1); }
-        mbar_init(bar(B_SEMPTY), 128);
+        mbar_init(bar(B_QEMPTY), 2);                  // one commit per score issuer
+        // score and value barriers per tile parity: each phase of one is waited for in
+        // order by the issuer or group that owns (or follows) those tiles
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_SFULL + i), 1);
+            mbar_init(bar(B_SEMPTY + i), 128);
+            mbar_init(bar(B_VDONE + i), 1);
+        }
         mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_OFREE), 128);
         for (int i = 0; i < 2; ++i) {
@@ -250,7 +258,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             mbar_init(bar(B_MH + i), 128);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_STATS + i), 256);
-        mbar_init(bar(B_FIN), 2);                     // one commit per MMA issuer
+        mbar_init(bar(B_FIN), 3);                     // one commit per MMA issuer
         *abort_flag = 0;
         fence_mbar_init_cluster();
     }
@@ -271,21 +279,52 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     // first thing in its own branch (80 + 168 + 168 + 96 = 4 x 128).
     if (warp < 4) reg_alloc_dec<80>();
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer + credits
+        // One thread serves two queues in an event loop: TMA loads of cache tiles into
+        // the ring, and the return of exchange buffers to the peer (a group that has read
+        // the peer's partial arrives on a local barrier; this thread, which has no remote
+        // stores of its own in flight, makes the cluster-scope release arrival).
         if (lane == 0) {
-            TileIt it;
-            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            TileIt ip, ic;                              // next tile to load, next credit
+            ip.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            ic.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            bool mp = ip.next(), mc = ic.next();
             uint32_t issued = 0;
-            while (it.next()) {
-                const uint32_t T = it.T, st = T % kStages;
-                if (!wait<false>(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1, ctl)) break;
-                const uint32_t dst = sStage + st * kStageBytes;
-                const int y = (int)(a.row_off[it.seg.b] + it.seg.lo + (int64_t)it.t * kTok);
-                mbar_expect_tx(bar(B_FULL + st), kStageBytes);
-                for (int j = 0; j < 4; ++j)
-                    tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
-                tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
-                issued = T + 1;
+            uint64_t t_prog = globaltimer_ns();
+            while (mp || mc) {
+                bool prog = false;
+                if (mp) {
+                    const uint32_t T = ip.T, st = T % kStages;
+                    if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
+                        const uint32_t dst = sStage + st * kStageBytes;
+                        const int y = (int)(a.row_off[ip.seg.b] + ip.seg.lo + (int64_t)ip.t * kTok);
+                        mbar_expect_tx(bar(B_FULL + st), kStageBytes);
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
+                        tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
+                        issued = T + 1;
+                        mp = ip.next();
+                        prog = true;
+                    }
+                }
+                if (mc) {
+                    const uint32_t T = ic.T;
+                    if (mbar_test_wait_cluster(bar(B_XCONS + (T & 1)), (T >> 1) & 1)) {
+                        mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
+                        mc = ic.next();
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    t_prog = globaltimer_ns();
+                } else {
+                    if (*abort_flag) break;
+                    if (globaltimer_ns() - t_prog > kTimeoutNs) {
+                        *abort_flag = 1;
+                        atomicOr(a.dev_status, MLA_DEV_TIMEOUT);
+                        break;
+                    }
+                }
             }
             // drain: every copy this thread issued has landed before the CTA may exit
             for (uint32_t k = 0; k < kStages && k < issued; ++k) {
@@ -293,67 +332,68 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
             }
         }
-    } else if (warp == 1 || warp == 2) {
-        // ------------------------------------------------------------ MMA issuers
-        // Warp 1 issues the score MMAs, warp 2 the value MMAs: two independent issue
-        // streams, so the score of tile T+1 never waits behind the value MMA of tile T
-        // (which waits for tile T's softmax).  The two touch disjoint tensor memory
-        // (S; O, P, Q'); a stage is released by the value MMA, which always completes
-        // after the score MMA of the same tile (the softmax in between needs it).
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ score MMA issuers
+        // Warp 1 issues the score MMAs of the even tiles into S[0], warp 3 those of the odd
+        // tiles into S[1]: two issue streams, so a score never waits for the previous
+        // tile's scores to be read.  With an even ring depth each stage, and so each
+        // FULL barrier, belongs to one issuer.  Both wait for every piece's Q' and both
+        // release it (QEMPTY counts two commits).
         if (lane == 0) {
+            const uint32_t par = warp == 1 ? 0u : 1u;
+            const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
+            const uint32_t sQR = base + kOffQR;
             TileIt it;
             it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
             bool ok = true;
-            if (warp == 1) {
-                const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
-                while (ok && it.next()) {
-                    const uint32_t T = it.T, st = T % kStages;
-                    if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
+            while (ok && it.next()) {
+                const uint32_t T = it.T;
+                if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
+                if ((T & 1u) == par) {
+                    const uint32_t st = T % kStages;
                     if (!(ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl))) break;
-                    if (T > 0 && !(ok = wait<false>(bar(B_SEMPTY), (T - 1) & 1, ctl))) break;
+                    if (T >= 2 && !(ok = wait<false>(bar(B_SEMPTY + par), ((T >> 1) - 1) & 1, ctl))) break;
                     tc_fence_after();
                     const uint32_t stage = sStage + st * kStageBytes;
-                    const uint32_t d = tmem + kColS;
+                    const uint32_t d = tmem + kColS + 64 * par;
                     for (int kk = 0; kk < 16; ++kk)
                         mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
                                     id_s, kk ? 1u : 0u);
                     for (int kk = 0; kk < 2; ++kk)
-                        mma_bf16_ts(d, tmem + kColQ + 8 * (16 + kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
-                    mma_commit(bar(B_SFULL + (T & 1)));
-                    if (it.last_tile()) mma_commit(bar(B_QEMPTY));
+                        mma_bf16(d, kdesc64(sQR + 32 * kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
+                    mma_commit(bar(B_SFULL + par));
                 }
-            } else {
-                const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
-                while (ok && it.next()) {
-                    const uint32_t T = it.T, st = T % kStages;
-                    if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
-                    if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
-                    tc_fence_after();
-                    const uint32_t stage = sStage + st * kStageBytes;
-                    for (int k = 0; k < kTok / 16; ++k)
-                        mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, mndesc128(stage + 2048 * k), id_o,
-                                    (it.first_tile() && k == 0) ? 0u : 1u);
-                    mma_commit(bar(B_EMPTY + st));
-                    mma_commit(bar(B_VDONE + (T & 1)));
-                }
+                if (it.last_tile()) mma_commit(bar(B_QEMPTY));
+            }
+            mma_commit(bar(B_FIN));
+            drain(bar(B_FIN), 0);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ value MMA issuer
+        // O_r += P C_r: P (bf16, 128 heads x 64 rows) from shared memory, the tile's
+        // latent half as an MN-major B operand.  A stage is released here: the value MMA
+        // of a tile always completes after its score MMA (the softmax in between needs it).
+        if (lane == 0) {
+            const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
+            const uint32_t sP = base + kOffP;
+            TileIt it;
+            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+            bool ok = true;
+            while (ok && it.next()) {
+                const uint32_t T = it.T, st = T % kStages;
+                if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
+                if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
+                tc_fence_after();
+                const uint32_t stage = sStage + st * kStageBytes;
+                for (int k = 0; k < kTok / 16; ++k)
+                    mma_bf16(tmem + kColO, kdesc128(sP + 32 * k), mndesc128(stage + 2048 * k), id_o,
+                             (it.first_tile() && k == 0) ? 0u : 1u);
+                mma_commit(bar(B_EMPTY + st));
+                mma_commit(bar(B_VDONE + (T & 1)));
             }
             // every MMA this thread issued has completed before the CTA may tear down
             mma_commit(bar(B_FIN));
             drain(bar(B_FIN), 0);
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ exchange credits
-        // Returns each exchange buffer to the peer once the owning group has read it.
-        // The groups signal a local barrier (cheap); this warp, which has no remote
-        // stores of its own in flight, makes the cluster-scope release arrival.
-        if (lane == 0) {
-            TileIt it;
-            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-            while (it.next()) {
-                const uint32_t T = it.T;
-                if (!wait<false>(bar(B_XCONS + (T & 1)), (T >> 1) & 1, ctl)) break;
-                mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
-            }
         }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ softmax / exchange
@@ -383,11 +423,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 float s[kTok];
                 if (!(ok = wwait<false>(bar(B_SFULL + xb), (T >> 1) & 1, ctl))) break;
                 tc_fence_after();
-                tmem_ld32(tmem + lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
-                tmem_ld32(tmem + lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+                tmem_ld32(tmem + lane_base + kColS + 64 * xb, *reinterpret_cast<float(*)[32]>(&s[0]));
+                tmem_ld32(tmem + lane_base + kColS + 64 * xb + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive(bar(B_SEMPTY));
+                mbar_arrive(bar(B_SEMPTY + xb));
                 // the peer has finished reading what this group sent for tile T - 2
                 if (T >= 2 && !(ok = wwait<true>(bar(B_XEMPTY + xb), ((T >> 1) - 1) & 1, ctl))) break;
                 if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
@@ -463,6 +503,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 }
                 mshare[(T & 1) * kHeads + i] = m_g;
                 mbar_arrive(bar(B_MH + (T & 1)));
+                // P tile (bf16) for the value MMA; the sum uses the rounded values
+                uint32_t packed[kTok / 2];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums (short chains)
+#pragma unroll
+                for (int j = 0; j < kTok / 2; ++j) {
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_g),
+                                                                    fast_exp2(s[2 * j + 1] - m_g));
+                    ls[j & 3] += __low2float(h2) + __high2float(h2);
+                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 // the value MMA of the previous tile has finished with P and O
                 if (T > 0) {
                     if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
@@ -479,18 +530,13 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         tmem_st16(tmem + lane_base + kColO + 16 * c, u);
                     }
                 }
-                // P tile (bf16) for the value MMA; the sum uses the rounded values
-                uint32_t packed[kTok / 2];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums (short chains)
+                {   // row i of P: 128 bytes, 16-byte chunk c stored at chunk c ^ (i & 7) (128B swizzle)
+                    uint8_t* prow = sm + kOffP + i * 128;
 #pragma unroll
-                for (int j = 0; j < kTok / 2; ++j) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_g),
-                                                                    fast_exp2(s[2 * j + 1] - m_g));
-                    ls[j & 3] += __low2float(h2) + __high2float(h2);
-                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                    for (int c = 0; c < 8; ++c)
+                        *(uint4*)(prow + ((c ^ (i & 7)) << 4)) =
+                            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
                 }
-                l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                tmem_st32u(tmem + lane_base + kColP, packed);
                 if (valid < kTok) {
                     // the value MMA must not see rows of the tile beyond the piece (they may
                     // hold anything): zero them in this CTA's latent half of the stage
@@ -499,8 +545,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
                         *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    fence_proxy_async_smem();
                 }
+                fence_proxy_async_smem();                   // P (and zeroed rows) to the tensor core
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(B_PFULL));
@@ -528,25 +574,29 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const bool row_ok = i < a.n_h;
             const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            // latent columns [256r, 256r + 256) in four chunks of 64 bf16 (32 TMEM columns)
+            {   // rotary columns [512 + 32r, 512 + 32r + 32): the A operand of the rotary
+                // score MMAs, in shared memory (row i: 64 bytes, 16-byte chunk c stored at
+                // chunk c ^ ((i >> 1) & 3), the 64B swizzle)
+                uint8_t* qrow = sm + kOffQR + i * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *(uint4*)(qrow + ((c ^ ((i >> 1) & 3)) << 4)) = row_ok ? src[64 + rank * 4 + c] : zero;
+                fence_proxy_async_smem();
+            }
+            // latent columns [256r, 256r + 256) into tensor memory, two chunks of 64 bf16
+            // (32 TMEM columns each) per round of loads
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
-                uint32_t r[32];
+            for (int k = 0; k < 4; k += 2) {
+                uint32_t r0[32], r1[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 v = row_ok ? src[rank * 32 + 8 * k + c] : zero;
-                    r[4 * c] = v.x; r[4 * c + 1] = v.y; r[4 * c + 2] = v.z; r[4 * c + 3] = v.w;
+                    const uint4 w = row_ok ? src[rank * 32 + 8 * k + 8 + c] : zero;
+                    r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
+                    r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
                 }
-                tmem_st32u(tmem + lane_base + kColQ + 32 * k, r);
-            }
-            {   // rotary columns [512 + 32r, 512 + 32r + 32)
-                uint32_t q[16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint4 v = row_ok ? src[64 + rank * 4 + c] : zero;
-                    q[4 * c] = v.x; q[4 * c + 1] = v.y; q[4 * c + 2] = v.z; q[4 * c + 3] = v.w;
-                }
-                tmem_st16(tmem + lane_base + kColQ + 128, q);
+                tmem_st32u(tmem + lane_base + kColQ + 32 * k, r0);
+                tmem_st32u(tmem + lane_base + kColQ + 32 * k + 32, r1);
             }
             tmem_wait_st();
             tc_fence_before();
