@@ -19,7 +19,8 @@ MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
             "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",
-            "mla_profile_events", "mla_append_workspace_size", "mla_decode_absorbed_noalloc")
+            "mla_profile_events", "mla_append_workspace_size", "mla_decode_absorbed_noalloc",
+            "mla_decode_prepare", "mla_decode_attend")
 
 
 class MlaDims(ctypes.Structure):
@@ -58,6 +59,9 @@ def load():
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
     lib.mla_decode_absorbed.restype = I32
+    for name in ("mla_decode_prepare", "mla_decode_attend"):
+        getattr(lib, name).argtypes = lib.mla_decode_absorbed.argtypes
+        getattr(lib, name).restype = I32
     lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P, P]
     lib.mla_decode_absorbed_noalloc.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, P, P, P]
     lib.mla_decode_absorbed_noalloc.restype = I32
@@ -132,6 +136,26 @@ def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, r
                         max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
                         stream=None):
     _check("mla_decode_absorbed", load().mla_decode_absorbed(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
+        _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
+
+
+def mla_decode_prepare(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len,
+                       max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                       stream=None):
+    """First half of mla_decode_absorbed: query fold, q_R rotation, schedule (no cache reads)."""
+    _check("mla_decode_prepare", load().mla_decode_prepare(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
+        _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
+
+
+def mla_decode_attend(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len,
+                      max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                      stream=None):
+    """Second half of mla_decode_absorbed: split-K attention over the cache and the merge."""
+    _check("mla_decode_attend", load().mla_decode_attend(
         ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
         _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
         _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))

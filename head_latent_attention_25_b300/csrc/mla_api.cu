@@ -6,6 +6,7 @@
 
 #include "mla_common.cuh"
 #include "mla_internal.h"
+#include "mla_schedule.cuh"
 
 using namespace mla;
 
@@ -195,12 +196,20 @@ size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t 
     return need;
 }
 
-mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
-                               const void* q_c, const void* q_r, const void* w_uk,
-                               const void* cache, int64_t cache_rows, const int64_t* row_off,
-                               const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
-                               void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
-                               int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+enum : int { kPrepare = 1, kAttend = 2 };
+
+// The decode in two phases: kPrepare (fold W_UK^T into the queries, rotate q_R, build the
+// schedule; reads no cache row) and kAttend (split-K attention over the cache, merge).
+mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                         const void* q_c, const void* q_r, const void* w_uk,
+                         const void* cache, int64_t cache_rows, const int64_t* row_off,
+                         const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                         void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                         int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || max_seq_len < 0 || num_splits < 0 || cache_rows < 1) return MLA_ERR_INVALID_ARG;
     if (!q_c || !q_r || !w_uk || !cache || !row_off || !seq_len || !o_lat || !dev_status)
@@ -223,16 +232,21 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
     float* part_l = (float*)(ws + p.ws.pl_off);
     const bool bf16 = dtype == MLA_BF16;
     const float alpha = scale_of(dims) * kLog2e;
-    cudaError_t e;
-    if (tc && gemm_tc_shapes_ok(*dims) && aligned(q_c, 16) && aligned(w_uk, 16)) {
-        e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s);
-        if (e == cudaSuccess) e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s);
-    } else {
-        e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
+    cudaError_t e = cudaSuccess;
+    if (phases & kPrepare) {
+        if (tc && gemm_tc_shapes_ok(*dims) && aligned(q_c, 16) && aligned(w_uk, 16)) {
+            // fold GEMM, then q_R rotation and the schedule in one launch
+            const ScheduleArgs sa{seq_len, row_off, cache_rows, batch, p.workers, cum, (Schedule*)sched, wstart,
+                                  dev_status};
+            e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s);
+            if (e == cudaSuccess) e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s, &sa);
+        } else {
+            e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
+            if (e == cudaSuccess)
+                e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, wstart, dev_status, s);
+        }
     }
-    if (e == cudaSuccess)
-        e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, wstart, dev_status, s);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && (phases & kAttend)) {
         if (tc)
             e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cache, cache_rows, row_off, cum,
                                 sched, wstart, o_lat, lse, part_o, part_l, dev_status, s);
@@ -240,10 +254,48 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
                                   sched, wstart, o_lat, lse, part_o, part_l, s);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && (phases & kAttend))
         e = launch_merge(*dims, bf16, batch, cum, sched, part_o, part_l, o_lat, lse, s);
     return cuda_status(e);
 }
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                               const void* q_c, const void* q_r, const void* w_uk,
+                               const void* cache, int64_t cache_rows, const int64_t* row_off,
+                               const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                               int32_t* dev_status, void* stream) {
+    return decode_phases(kPrepare | kAttend, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                         seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                         stream);
+}
+
+mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                              const void* q_c, const void* q_r, const void* w_uk,
+                              const void* cache, int64_t cache_rows, const int64_t* row_off,
+                              const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                              void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                              int32_t* dev_status, void* stream) {
+    return decode_phases(kPrepare, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                         seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                         stream);
+}
+
+mla_status mla_decode_attend(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                             const void* q_c, const void* q_r, const void* w_uk,
+                             const void* cache, int64_t cache_rows, const int64_t* row_off,
+                             const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                             void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                             int32_t* dev_status, void* stream) {
+    return decode_phases(kAttend, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                         seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                         stream);
+}
+
 
 mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o_lat,
                            const void* w_uv, void* out, int32_t* dev_status, void* stream) {

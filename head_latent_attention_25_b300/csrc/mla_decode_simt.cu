@@ -9,78 +9,14 @@
 
 #include "mla_common.cuh"
 #include "mla_internal.h"
+#include "mla_schedule.cuh"
 
 namespace mla {
 
 namespace {
 
 // ------------------------------------------------------------------ schedule
-// A sequence takes part with its length when 1 <= seq_len and its rows lie inside the
-// cache buffer; otherwise it counts as empty and MLA_DEV_BAD_LENGTH is raised.
-__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* seq_len,
-                                                        const int64_t* row_off, int64_t cache_rows,
-                                                        int batch, int workers, int64_t* cum,
-                                                        Schedule* sched, int32_t* wstart,
-                                                        int32_t* dev_status) {
-    __shared__ long long warp_tot[32];
-    __shared__ long long carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) carry = 0;
-    __syncthreads();
-    for (int base = 0; base < batch; base += 1024) {
-        const int i = base + tid;
-        long long x = 0;
-        if (i < batch) {
-            const long long n = seq_len[i], o = row_off[i];
-            if (n >= 1 && o >= 0 && o + n <= cache_rows) x = n;
-            else atomicOr(dev_status, MLA_DEV_BAD_LENGTH);
-        }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            long long y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            long long t = warp_tot[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                long long y = __shfl_up_sync(0xffffffffu, t, o);
-                if (lane >= o) t += y;
-            }
-            warp_tot[lane] = t;
-        }
-        __syncthreads();
-        const long long incl = carry + (warp ? warp_tot[warp - 1] : 0) + x;
-        if (i < batch) cum[i + 1] = incl;
-        __syncthreads();
-        if (tid == 1023) carry = incl;
-        __syncthreads();
-    }
-    if (tid == 0) {
-        cum[0] = 0;
-        Schedule s;
-        s.total = carry;
-        s.workers = workers;
-        s.batch = batch;
-        s.per = carry > 0 ? (carry + workers - 1) / workers : 1;
-        *sched = s;
-    }
-    __syncthreads();                            // cum complete and visible to the block
-    // first sequence of each worker's range: the last sequence whose rows start at or
-    // before the range start (saves every role of the split kernels a binary search)
-    const int64_t per = carry > 0 ? (carry + workers - 1) / workers : 1;
-    for (int g = tid; g < workers; g += 1024) {
-        const int64_t cur = (int64_t)g * per;
-        int lo = 0, hi = batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (cum[mid] <= cur) lo = mid; else hi = mid - 1;
-        }
-        wstart[g] = lo;
-    }
-}
+__global__ void __launch_bounds__(1024) schedule_kernel(ScheduleArgs a) { build_schedule(a); }
 
 // ------------------------------------------------------------------ SIMT split
 constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
@@ -294,8 +230,8 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
 cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
                             int batch, int workers, int64_t* cum, void* sched, int32_t* wstart,
                             int32_t* dev_status, cudaStream_t s) {
-    schedule_kernel<<<1, 1024, 0, s>>>(seq_len, row_off, cache_rows, batch, workers, cum,
-                                       (Schedule*)sched, wstart, dev_status);
+    ScheduleArgs a{seq_len, row_off, cache_rows, batch, workers, cum, (Schedule*)sched, wstart, dev_status};
+    schedule_kernel<<<1, 1024, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

@@ -28,8 +28,12 @@ cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const vo
                                const void* w_uv, void* out, cudaStream_t s);
 
 // The rotary part of Q' alone (the content part comes from a GEMM).
+struct ScheduleArgs;
+// q_R rotation into Q'; with sched_args it also builds the split schedule (one extra
+// block column), otherwise launch_schedule does.
 cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
-                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s);
+                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s,
+                             const ScheduleArgs* sched_args);
 
 // tcgen05 projections (bf16; shapes accepted by gemm_tc_shapes_ok)
 bool gemm_tc_shapes_ok(const mla_dims& d);

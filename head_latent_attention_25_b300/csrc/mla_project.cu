@@ -4,6 +4,7 @@
 // accumulation; they differ only in strides and in what the epilogue does.
 #include "mla_common.cuh"
 #include "mla_internal.h"
+#include "mla_schedule.cuh"
 
 namespace mla {
 
@@ -144,9 +145,16 @@ template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) fold_rope_kernel(const Tin* __restrict__ q_r,
                                                         const int32_t* __restrict__ seq_len,
                                                         Tout* __restrict__ qp, int n_h, int d_c,
-                                                        int d_r, double rope_r, float alpha) {
+                                                        int d_r, double rope_r, float alpha,
+                                                        ScheduleArgs sch) {
     __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
     const int b = blockIdx.x;
+    if (b == gridDim.x - 1 && sch.cum) {
+        // one extra column of blocks: its first block builds the split schedule, which
+        // saves the decode a launch (it depends only on seq_len and row_off)
+        if (blockIdx.y == 0) build_schedule(sch);
+        return;
+    }
     const int h0 = blockIdx.y * kRopeHeads;
     const int half = d_r / 2;
     const int n_heads = min(kRopeHeads, n_h - h0);
@@ -208,24 +216,27 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
     a.alpha = alpha;
     cudaError_t e = dispatch(a, in_bf16, out_bf16, s);
     if (e != cudaSuccess) return e;
-    return launch_fold_rope(d, in_bf16, out_bf16, batch, q_r, seq_len, alpha, qp, s);
+    return launch_fold_rope(d, in_bf16, out_bf16, batch, q_r, seq_len, alpha, qp, s, nullptr);
 }
 
 cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
-                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s) {
+                             const int32_t* seq_len, float alpha, void* qp, cudaStream_t s,
+                             const ScheduleArgs* sched_args) {
     if (d.d_r / 2 > kMaxRopePairs) return cudaErrorInvalidValue;
-    const dim3 grid(batch, (d.n_heads + kRopeHeads - 1) / kRopeHeads);
+    ScheduleArgs sch{};
+    if (sched_args) sch = *sched_args;
+    const dim3 grid(batch + (sched_args ? 1 : 0), (d.n_heads + kRopeHeads - 1) / kRopeHeads);
     const double r = rope_ratio(d.rope_base, d.d_r);
     if (in_bf16) {
         if (out_bf16)
             fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, r, alpha);
+                (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
         else
             fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha);
+                (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
     } else {
         fold_rope_kernel<<<grid, 256, 0, s>>>((const float*)q_r, seq_len, (float*)qp,
-            d.n_heads, d.d_c, d.d_r, r, alpha);
+            d.n_heads, d.d_c, d.d_r, r, alpha, sch);
     }
     note_launch();
     return cudaGetLastError();

@@ -1,0 +1,86 @@
+// The split schedule of the decode: prefix sums of the sequence lengths over the
+// flattened context, the equal share of rows per worker, and each worker's first
+// sequence.  Built by one thread block of any size (a multiple of 32, at most 1024).
+#pragma once
+
+#include "mla_common.cuh"
+
+namespace mla {
+
+struct ScheduleArgs {
+    const int32_t* seq_len;
+    const int64_t* row_off;
+    int64_t cache_rows;
+    int batch;
+    int workers;
+    int64_t* cum;           // [batch + 1]
+    Schedule* sched;
+    int32_t* wstart;        // [workers]
+    int32_t* dev_status;
+};
+
+// A sequence takes part with its length when 1 <= seq_len and its rows lie inside the
+// cache buffer; otherwise it counts as empty and MLA_DEV_BAD_LENGTH is raised.
+__device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
+    __shared__ long long warp_tot[32];
+    __shared__ long long carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < a.batch; base += nt) {
+        const int i = base + tid;
+        long long x = 0;
+        if (i < a.batch) {
+            const long long n = a.seq_len[i], o = a.row_off[i];
+            if (n >= 1 && o >= 0 && o + n <= a.cache_rows) x = n;
+            else atomicOr(a.dev_status, MLA_DEV_BAD_LENGTH);
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long t = lane < nt / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                long long y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const long long incl = carry + (warp ? warp_tot[warp - 1] : 0) + x;
+        if (i < a.batch) a.cum[i + 1] = incl;
+        __syncthreads();
+        if (tid == nt - 1) carry = incl;
+        __syncthreads();
+    }
+    const long long total = carry;
+    const int64_t per = total > 0 ? (total + a.workers - 1) / a.workers : 1;
+    if (tid == 0) {
+        a.cum[0] = 0;
+        Schedule s;
+        s.total = total;
+        s.workers = a.workers;
+        s.batch = a.batch;
+        s.per = per;
+        *a.sched = s;
+    }
+    __syncthreads();                            // cum complete and visible to the block
+    // first sequence of each worker's range: the last sequence whose rows start at or
+    // before the range start (saves every role of the split kernels a binary search)
+    for (int g = tid; g < a.workers; g += nt) {
+        const int64_t cur = (int64_t)g * per;
+        int lo = 0, hi = a.batch - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.cum[mid] <= cur) lo = mid; else hi = mid - 1;
+        }
+        a.wstart[g] = lo;
+    }
+}
+
+}  // namespace mla

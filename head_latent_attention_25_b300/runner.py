@@ -65,6 +65,7 @@ class DecodeStep:
         self.app_ws_bytes = L.mla_append_workspace_size(self.dims, self.dt, B, n_new)
         self.app_workspace = torch.empty(max(self.app_ws_bytes, 256), dtype=torch.uint8, device=device)
         self.w = {}
+        self.side = torch.cuda.Stream(device=device)     # the cache append runs here, see step()
 
     # ------------------------------------------------------------------ inputs
     def set_weights(self, weights: dict):
@@ -108,12 +109,42 @@ class DecodeStep:
                               ws.numel(), self.o_lat if o_lat is None else o_lat,
                               self.lse if lse is None else lse, self.dev_status, stream)
 
+    def _decode_args(self):
+        return (self.dims, self.dt, self.batch, self.q_c, self.q_r, self.w["w_uk"], self.cache,
+                self.total_rows, self.row_off, self.seq_len, self.max_seq_len, self.num_splits,
+                self.workspace, self.workspace.numel(), self.o_lat, self.lse, self.dev_status)
+
+    def decode_prepare(self, stream=None):
+        """Query fold, q_R rotation and schedule into the workspace; reads no cache row."""
+        L.mla_decode_prepare(*self._decode_args(), stream)
+
+    def decode_attend(self, stream=None):
+        """Attention over the cache and merge, from what decode_prepare left in the workspace."""
+        L.mla_decode_attend(*self._decode_args(), stream)
+
     def project_out(self, stream=None):
         L.mla_project_out(self.dims, self.dt, self.batch, self.o_lat, self.w["w_uv"], self.out,
                           self.dev_status, stream)
 
     def step(self, stream=None):
-        """The whole path: append, [query projection], decode, up-projection."""
+        """The whole path: append, [query projection], decode, up-projection.
+
+        The cache append and the query-side half of the decode are independent (the fold
+        reads no cache row), so the append runs on a second stream beside it; the attention
+        waits for both.  Under stream capture this becomes two branches of the graph.
+        """
+        main = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(self.device)
+        self.side.wait_stream(main)             # this step's inputs, and earlier reads of the cache
+        self.append(self.side)
+        if self.query_from_h:
+            self.project_query(main)
+        self.decode_prepare(main)
+        main.wait_stream(self.side)
+        self.decode_attend(main)
+        self.project_out(main)
+
+    def step_serial(self, stream=None):
+        """The same path as step(), every call on one stream."""
         self.append(stream)
         if self.query_from_h:
             self.project_query(stream)

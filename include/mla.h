@@ -178,6 +178,33 @@ MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, in
                                void* o_lat, float* lse, int32_t* dev_status, void* stream);
 
 /*
+ * mla_decode_prepare, mla_decode_attend -- mla_decode_absorbed in two calls, so that the
+ * query-side work can run beside the cache append of the same step (the fold reads no
+ * cache row).  Both take exactly the arguments of mla_decode_absorbed, and the two calls
+ * together have exactly its effect:
+ *   mla_decode_prepare  folds W_UK^T into the queries, rotates q_r and builds the split
+ *                       schedule, all into `workspace`; it reads q_c, q_r, w_uk, row_off and
+ *                       seq_len but no cache row, and writes neither o_lat nor lse;
+ *   mla_decode_attend   runs the split-K attention over the cache and the merge, reading
+ *                       what mla_decode_prepare left in `workspace`; it must follow that
+ *                       call in stream order, with identical arguments and an untouched
+ *                       workspace, and after every cache row it attends over is written.
+ * Errors and dev_status flags are those of mla_decode_absorbed.
+ */
+MLA_API mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                              const void* q_c, const void* q_r, const void* w_uk,
+                              const void* cache, int64_t cache_rows, const int64_t* row_off,
+                              const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                              void* workspace, size_t workspace_bytes,
+                              void* o_lat, float* lse, int32_t* dev_status, void* stream);
+MLA_API mla_status mla_decode_attend(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                             const void* q_c, const void* q_r, const void* w_uk,
+                             const void* cache, int64_t cache_rows, const int64_t* row_off,
+                             const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                             void* workspace, size_t workspace_bytes,
+                             void* o_lat, float* lse, int32_t* dev_status, void* stream);
+
+/*
  * mla_project_out -- o_i = W_UV^(i) o_lat_i for every head ("Grouped-query and
  * latent attention", section "The absorption trick", value side).
  *

@@ -64,6 +64,11 @@ def test_null_pointers_rejected_on_host():
                                    1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_absorbed(ctypes.byref(d), 0, 1, fake, fake, fake, fake, 0, fake, fake, 8, 1, fake,
                                    1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
+    for fn in (lib.mla_decode_prepare, lib.mla_decode_attend):
+        assert fn(ctypes.byref(d), 0, 1, fake, fake, fake, None, 64, fake, fake, 8, 1, fake,
+                  1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
+        assert fn(ctypes.byref(d), 0, 1, fake, fake, fake, fake, 64, fake, fake, 8, 1, None,
+                  1 << 20, fake, None, fake, None) == mla.MLA_ERR_WORKSPACE
     assert lib.mla_project_query(ctypes.byref(d), 0, 1, 64, fake, fake, None, fake, fake,
                                  None) == mla.MLA_ERR_INVALID_ARG
     assert lib.mla_cache_append(None, 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,

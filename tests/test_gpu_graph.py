@@ -53,3 +53,20 @@ def test_graph_follows_new_queries():
     assert int(st.dev_status.item()) == 0
     assert not torch.equal(replayed, first)
     assert torch.equal(replayed, st.out)
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "tiny_f32"])
+def test_two_stream_step_matches_one_stream(name):
+    """step() runs the cache append on a second stream beside the query fold
+    (mla_decode_prepare), then the attention (mla_decode_attend); the results equal
+    those of the whole path on one stream, appended rows included."""
+    wl = mla_inputs.WORKLOADS[name]
+    a = runner.from_workload(wl)
+    b = runner.from_workload(wl)
+    a.step()
+    b.step_serial()
+    torch.cuda.synchronize()
+    assert int(a.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
+    assert torch.equal(a.cache, b.cache)
+    for x, y in ((a.o_lat, b.o_lat), (a.lse, b.lse), (a.out, b.out)):
+        assert torch.equal(x, y)
