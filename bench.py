@@ -188,6 +188,31 @@ def config_of(wl, lens, extra=None):
 
 
 # ---------------------------------------------------------------- our arm
+# ---------------------------------------------------------------- multi-rank timing
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it).  Replicas only: the ranks run
+    independent copies of the workload and exchange nothing but this number."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def job_throughput(units_per_rank: int, world: int, steps: int, ms_max: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * world * steps / (ms_max / 1e3)
+
+
 def run_ours(args, wl, rank, world):
     import torch
     import torch.distributed as dist
@@ -200,16 +225,6 @@ def run_ours(args, wl, rank, world):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -228,7 +243,7 @@ def run_ours(args, wl, rank, world):
         a.record(stream)
         b.record(stream)
     t_beg, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     n0 = mla_launch_count()
     wall0 = time.time()
@@ -239,10 +254,10 @@ def run_ours(args, wl, rank, world):
     t_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
-    barrier()
+    barrier(world)
     mla_profile_events(None, None)
     launches = mla_launch_count() - n0
-    ms_eager = max_over_ranks(t_beg.elapsed_time(t_end))
+    ms_eager = max_over_ranks(t_beg.elapsed_time(t_end), world)
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_split)
     assert int(st.dev_status.item()) == 0
 
@@ -255,7 +270,7 @@ def run_ours(args, wl, rank, world):
         for _ in range(args.warmup):
             g.replay()
         g_beg, g_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
+        barrier(world)
         torch.cuda.synchronize()
         g_beg.record(stream)
         for _ in range(K):
@@ -263,9 +278,9 @@ def run_ours(args, wl, rank, world):
         g_end.record(stream)
         torch.cuda.synchronize()
         wall1 = time.time()
-        barrier()
+        barrier(world)
         assert int(st.dev_status.item()) == 0
-        ms_graph = max_over_ranks(g_beg.elapsed_time(g_end))
+        ms_graph = max_over_ranks(g_beg.elapsed_time(g_end), world)
     clocks = ClockSampler.summary(sampler.stop(), wall0, wall1) if sampler else None
     ms = ms_graph if ms_graph is not None else ms_eager
 
@@ -295,15 +310,15 @@ def run_ours(args, wl, rank, world):
     for _ in range(args.warmup):
         e2e_step()
     e_beg, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     e_beg.record(stream)
     for _ in range(K):
         e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(e_beg.elapsed_time(e_end))
+    barrier(world)
+    e2e_ms = max_over_ranks(e_beg.elapsed_time(e_end), world)
 
     if rank != 0:
         return None
@@ -312,8 +327,7 @@ def run_ours(args, wl, rank, world):
     split_s = split_ms / 1e3
     gbs = cache_bytes / split_s / 1e9
     tfs = flops / split_s / 1e12
-    tokens = wl.batch * world * K
-    value = tokens / (ms / 1e3)
+    value = job_throughput(wl.batch, world, K, ms)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
@@ -330,7 +344,7 @@ def run_ours(args, wl, rank, world):
                             "peak_sustained": tf_sus, "frac_burst": tfs / tf_burst,
                             "frac_sustained": tfs / tf_sus, "algorithmic_flops_per_launch": flops},
         "cache_gbs_step": cache_bytes / (ms / K / 1e3) / 1e9,
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(wl.batch, world, K, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "launch": "cuda_graph" if g is not None else "eager"},
         "gpu_launches": launches,
         "clocks": clocks,
