@@ -253,7 +253,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         mbar_init(bar(B_OFREE), 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_XFULL + i), 1);
-            mbar_init(bar(B_XEMPTY + i), 1);            // the peer's credit warp
+            mbar_init(bar(B_XEMPTY + i), 1);            // one credit from the peer's producer thread
             mbar_init(bar(B_XCONS + i), 128);           // this CTA's group has read X[i]
             mbar_init(bar(B_MH + i), 128);
         }
