@@ -70,3 +70,20 @@ def test_two_stream_step_matches_one_stream(name):
     assert torch.equal(a.cache, b.cache)
     for x, y in ((a.o_lat, b.o_lat), (a.lse, b.lse), (a.out, b.out)):
         assert torch.equal(x, y)
+
+
+def test_prepare_reads_no_cache_row():
+    """mla_decode_prepare may run before the new rows are in the cache: prepare, then
+    append, then attend (one stream) gives the same results as the whole step."""
+    wl = mla_inputs.WORKLOADS["small_bf16"]
+    a = runner.from_workload(wl)
+    b = runner.from_workload(wl)
+    a.decode_prepare()
+    a.append()
+    a.decode_attend()
+    a.project_out()
+    b.step_serial()
+    torch.cuda.synchronize()
+    assert int(a.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
+    for x, y in ((a.cache, b.cache), (a.o_lat, b.o_lat), (a.lse, b.lse), (a.out, b.out)):
+        assert torch.equal(x, y)
