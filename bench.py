@@ -288,17 +288,13 @@ def run_ours(args, wl, rank, world):
     # to pinned host memory, as in a serving loop: the copies run on a second stream through
     # double-buffered device staging, so step k+1's inputs and step k-1's result move while
     # step k computes; every step still carries its own copies.
-    h_host = st.h.cpu().pin_memory()
-    qc_host, qr_host = st.q_c.cpu().pin_memory(), st.q_r.cpu().pin_memory()
-    h2d = h_host.numel() * h_host.element_size()
-    if not wl.query_from_h:
-        h2d += qc_host.numel() * qc_host.element_size() + qr_host.numel() * qr_host.element_size()
+    # h, q_c and q_r are views of one contiguous device buffer (st.inputs): one copy each way
+    in_host = st.inputs.cpu().pin_memory()
+    h2d = in_host.numel() * in_host.element_size()
     d2h = st.out.numel() * st.out.element_size()
     NS = 2
     copy_stream = torch.cuda.Stream()
-    stage_h = [torch.empty_like(st.h) for _ in range(NS)]
-    stage_qc = [torch.empty_like(st.q_c) for _ in range(NS)]
-    stage_qr = [torch.empty_like(st.q_r) for _ in range(NS)]
+    stage_in = [torch.empty_like(st.inputs) for _ in range(NS)]
     stage_out = [torch.empty_like(st.out) for _ in range(NS)]
     out_host = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(NS)]
     ev_in = [torch.cuda.Event() for _ in range(NS)]      # inputs of the slot are on the device
@@ -311,21 +307,15 @@ def run_ours(args, wl, rank, world):
         with torch.cuda.stream(copy_stream):
             if used[sl]:
                 copy_stream.wait_event(ev_used[sl])      # step k-NS has read this slot
-            stage_h[sl].copy_(h_host, non_blocking=True)
-            if not wl.query_from_h:
-                stage_qc[sl].copy_(qc_host, non_blocking=True)
-                stage_qr[sl].copy_(qr_host, non_blocking=True)
+            stage_in[sl].copy_(in_host, non_blocking=True)
             ev_in[sl].record(copy_stream)
 
     def compute(k):
         sl = k % NS
         stream.wait_event(ev_in[sl])
-        st.h.copy_(stage_h[sl])
+        st.inputs.copy_(stage_in[sl])
         if wl.query_from_h:
             st.x_q.copy_(st.h[:, -1, :])
-        else:
-            st.q_c.copy_(stage_qc[sl])
-            st.q_r.copy_(stage_qr[sl])
         if g is not None:
             g.replay()
         else:

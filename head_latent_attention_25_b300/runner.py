@@ -49,9 +49,17 @@ class DecodeStep:
         self.seq_len = torch.tensor([c + n_new for c in self.ctx_lens], dtype=torch.int32, device=device)
         self.max_seq_len = max(c + n_new for c in self.ctx_lens)
         self.cache = torch.zeros(self.total_rows, self.row_elems, dtype=self.tdt, device=device)
-        self.h = torch.zeros(B, n_new, hidden, dtype=self.tdt, device=device)
-        self.q_c = torch.zeros(B, n_heads, d_h, dtype=self.tdt, device=device)
-        self.q_r = torch.zeros(B, n_heads, d_r, dtype=self.tdt, device=device)
+        # the step's inputs h, q_c, q_r are views of one contiguous buffer (each part starts
+        # on a 256-byte boundary), so a caller can move them with one copy
+        def _round(n):
+            return (n + 127) // 128 * 128
+        n_h, n_c, n_r = B * n_new * hidden, B * n_heads * d_h, B * n_heads * d_r
+        o_c = _round(n_h)
+        o_r = o_c + _round(n_c)
+        self.inputs = torch.zeros(o_r + _round(n_r), dtype=self.tdt, device=device)
+        self.h = self.inputs[:n_h].view(B, n_new, hidden)
+        self.q_c = self.inputs[o_c:o_c + n_c].view(B, n_heads, d_h)
+        self.q_r = self.inputs[o_r:o_r + n_r].view(B, n_heads, d_r)
         self.x_q = torch.zeros(B, self.d_q_in, dtype=self.tdt, device=device) if query_from_h else None
         self.o_lat = torch.zeros(B, n_heads, d_c, dtype=self.tdt, device=device)
         self.lse = torch.zeros(B, n_heads, dtype=torch.float32, device=device)
