@@ -176,12 +176,30 @@ def workload_facts(wl, lens):
     return rows, rows * row_bytes, rows * flops_per_row
 
 
+L2_BYTES = 126 * 2 ** 20
+
+
+def step_footprint(wl, lens):
+    """Bytes a step reads from memory: the attended cache rows plus the weights."""
+    el = 2 if wl.dtype == "bf16" else 4
+    _, cache_bytes, _ = workload_facts(wl, lens)
+    weights = ((wl.d_c + wl.d_r) * wl.hidden + 2 * wl.n_heads * wl.d_h * wl.d_c) * el
+    return cache_bytes + weights
+
+
+def l2_note(wl, lens):
+    mb = step_footprint(wl, lens) / 1e6
+    if step_footprint(wl, lens) > L2_BYTES:
+        return f"inputs larger than L2 ({mb:.0f} MB of cache rows and weights per step); no flush"
+    return (f"inputs fit in L2 ({mb:.1f} MB of cache rows and weights per step); no flush, "
+            f"so repeated steps read them from L2")
+
+
 def config_of(wl, lens, extra=None):
     c = {"workload": wl.name, "batch": wl.batch, "n_heads": wl.n_heads, "d_h": wl.d_h, "d_c": wl.d_c,
          "d_r": wl.d_r, "hidden": wl.hidden, "context_rows": (lens[0] if wl.ragged is None else
                                                                [int(min(lens)), int(max(lens))]),
-         "new_tokens_per_seq": wl.n_new, "seed": wl.seed,
-         "l2": "inputs larger than L2 (latent cache plus weights exceed 126 MB); no flush"}
+         "new_tokens_per_seq": wl.n_new, "seed": wl.seed, "l2": l2_note(wl, lens)}
     if extra:
         c.update(extra)
     return c
