@@ -16,12 +16,10 @@ replica of the workload (weak scaling; the path has no exchange step).
 from __future__ import annotations
 
 import argparse
-import datetime
 import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -48,6 +46,8 @@ def parse():
     p.add_argument("--no-graph", action="store_true",
                    help="time eager launches only (default: the step captured once into a CUDA graph)")
     p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--no-from-h", action="store_true",
+                   help="skip the companion measurement of the step with the query computed from h")
     return p.parse_args()
 
 
@@ -62,51 +62,90 @@ def peaks():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons, kept with their times."""
-    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
-              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    """SM clock and clock-event (throttle) reasons of one GPU, read through NVML by a
+    host thread every ~2 ms and kept with their wall times, so that even a timed region
+    of a few milliseconds holds samples.  Read-only: no setting of the GPU is touched.
+    When NVML cannot be used the reason is kept in ``error`` and reported."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
 
-    def __init__(self, device_id: str):
-        self.proc = None
+    def __init__(self, uuid: str, period_s: float = 0.002):
+        import threading
+        self.rows, self.error, self.period = [], None, period_s
+        self._stop = threading.Event()
+        self._thread = None
+        self.source = "nvml"
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", device_id, "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self._max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
+            target = self._run
+        except Exception as e:                     # no NVML binding: nvidia-smi in a loop
+            self.error = f"nvml unavailable ({type(e).__name__}); nvidia-smi every 20 ms"
+            self.source, self.period, self._uuid = "nvidia-smi", 0.02, uuid
+            target = self._run_smi
+        self._thread = threading.Thread(target=target, daemon=True)
+        self._thread.start()
+
+    def _run_smi(self):
+        import subprocess
+        fields = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active"]
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", self._uuid, "--query-gpu=" + ",".join(fields),
+                                     "--format=csv,noheader,nounits", "-lms", "20"],
+                                    stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        except Exception as e:
+            self.error = f"nvidia-smi failed: {type(e).__name__}: {e}"
+            return
+        while not self._stop.is_set():
+            line = proc.stdout.readline()
+            if not line:
+                self.error = "nvidia-smi ended: " + (proc.stderr.read() or "")[:200]
+                break
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                self.rows.append((time.time(), float(parts[0]), float(parts[1]), int(parts[2], 16)))
+            except (ValueError, IndexError):
+                continue
+        proc.terminate()
+        try:
+            proc.wait(timeout=5)
         except Exception:
-            self.proc = None
+            proc.kill()
+
+    def _run(self):
+        nv, h = self._nv, self._h
+        while not self._stop.is_set():
+            try:
+                t = time.time()
+                sm = float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
+                r = int(nv.nvmlDeviceGetCurrentClocksEventReasons(h))
+                self.rows.append((t, sm, self._max, r))
+            except Exception as e:
+                self.error = f"nvml read failed: {type(e).__name__}: {e}"
+                return
+            time.sleep(self.period)
 
     def stop(self):
-        if self.proc is None:
-            return []
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = []
-        for line in out.splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) != len(self.FIELDS):
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
-            except ValueError:
-                continue
-        return rows
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+        return self.rows
 
-    @staticmethod
-    def summary(rows, t0, t1):
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sel = [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.05]
+    def summary(self, windows):
+        """Median SM clock and the union of active reasons over the samples taken inside
+        the given (t0, t1) wall-time windows."""
+        sel = [r for r in self.rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)]
+        span = sum(t1 - t0 for t0, t1 in windows)
         if not sel:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window_s": span, "source": self.source, "error": self.error or "no sample in the window"}
+        reasons = sorted({n for r in sel for n, bit in self.REASONS if r[3] & bit})
         return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
-                "reasons": reasons, "samples": len(sel)}
+                "reasons": reasons, "samples": len(sel), "window_s": span,
+                "source": f"{self.source} every {self.period * 1e3:.0f} ms during the timed loops"}
 
 
 # ---------------------------------------------------------------- evidence from ncu
@@ -177,6 +216,7 @@ def workload_facts(wl, lens):
 
 
 L2_BYTES = 126 * 2 ** 20
+NOMINAL_HBM_GBS = 8000.0             # "about 8 TB/s", the nominal HBM3e figure
 
 
 def step_footprint(wl, lens):
@@ -231,6 +271,86 @@ def job_throughput(units_per_rank: int, world: int, steps: int, ms_max: float) -
     return units_per_rank * world * steps / (ms_max / 1e3)
 
 
+# Workloads whose step is also measured with the query computed on the GPU from the new
+# token's h (c_q = W_DQ h, q_C = W_UQ c_q, q_R = W_QR c_q) instead of given q_C, q_R.
+FROM_H = {"v3_b64_l4096": "v3_b64_l4096_from_h"}
+
+
+def time_from_h(args, name):
+    """Graph-replay time of the h -> o step of workload ``name`` (mean of K replays)."""
+    import torch
+    import mla_inputs
+    from head_latent_attention_25_b300 import runner
+    wl = mla_inputs.WORKLOADS[name]
+    lens = mla_inputs.context_lengths(wl)
+    st = runner.from_workload(wl, ctx_lens=lens, num_splits=args.num_splits)
+    g = st.capture()
+    for _ in range(args.warmup):
+        g.replay()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) == 0
+    ms = a.elapsed_time(b) / args.steps
+    el = 2 if wl.dtype == "bf16" else 4
+    q_weights = (wl.d_q * wl.hidden + wl.n_heads * (wl.d_h + wl.d_r) * wl.d_q) * el
+    out = {"workload": name, "ms_per_step": ms, "value": wl.batch / (ms / 1e3), "unit": UNIT,
+           "query_weight_bytes": q_weights,
+           "path": "c_q = W_DQ h, [q_C; q_R] = [W_UQ; W_QR] c_q, then the same step (graph replay)"}
+    del st, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_output_forms(args, name):
+    """The layer output after the step, u = W_O [o_1; ...; o_n_h], timed two ways (mean of
+    K launches each, CUDA events): two-step (W_UV per head, then W_O) and with W_UV merged
+    into W_O (W_OV applied to the latent output)."""
+    import dataclasses
+    import torch
+    import mla_inputs
+    from head_latent_attention_25_b300 import runner
+    wl = dataclasses.replace(mla_inputs.WORKLOADS[name], name=name + "_out", w_o=True)
+    st = runner.from_workload(wl, num_splits=args.num_splits)
+    st.step()
+    st.merge_output_weights()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    def two_step():
+        st.project_out()
+        st.project_output()
+
+    ms_two, ms_merged = timed(two_step), timed(st.project_output_merged)
+    assert int(st.dev_status.item()) == 0
+    el = 2 if wl.dtype == "bf16" else 4
+    w_two = wl.n_heads * wl.d_h * (wl.d_c + wl.hidden) * el
+    w_merged = wl.n_heads * wl.d_c * wl.hidden * el
+    out = {"workload": wl.name, "two_step_ms": ms_two, "merged_ms": ms_merged,
+           "two_step_weight_bytes": w_two, "merged_weight_bytes": w_merged,
+           "two_step_gbs": w_two / (ms_two / 1e3) / 1e9, "merged_gbs": w_merged / (ms_merged / 1e3) / 1e9}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl, rank, world):
     import torch
     import torch.distributed as dist
@@ -254,6 +374,7 @@ def run_ours(args, wl, rank, world):
         st.step()
     torch.cuda.synchronize()
     assert int(st.dev_status.item()) == 0, "device status set during warm-up"
+    windows = []                        # wall-time windows of the timed loops (clock record)
 
     K = args.steps
     ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -271,18 +392,20 @@ def run_ours(args, wl, rank, world):
         st.step()
     t_end.record(stream)
     torch.cuda.synchronize()
-    wall1 = time.time()
+    windows.append((wall0, time.time()))
     barrier(world)
     mla_profile_events(None, None)
     launches = mla_launch_count() - n0
     ms_eager = max_over_ranks(t_beg.elapsed_time(t_end), world)
-    split_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_split)
+    split_times = [a.elapsed_time(b) for a, b in ev_split]
+    split_ms = statistics.mean(split_times)
     assert int(st.dev_status.item()) == 0
 
     # the same step captured once into a CUDA graph and replayed K times (the kernels
     # and their arguments are identical; only the host launch path differs)
     ms_graph = None
     g = None
+    replay_ms = []
     if not args.no_graph:
         g = st.capture()
         for _ in range(args.warmup):
@@ -290,29 +413,49 @@ def run_ours(args, wl, rank, world):
         g_beg, g_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
+        wall0 = time.time()
         g_beg.record(stream)
         for _ in range(K):
             g.replay()
         g_end.record(stream)
         torch.cuda.synchronize()
-        wall1 = time.time()
+        windows.append((wall0, time.time()))
         barrier(world)
         assert int(st.dev_status.item()) == 0
         ms_graph = max_over_ranks(g_beg.elapsed_time(g_end), world)
-    clocks = ClockSampler.summary(sampler.stop(), wall0, wall1) if sampler else None
+        # per-replay durations for the median: at least 50 replays and at least 0.5 s,
+        # each bracketed by events recorded between consecutive replays
+        n_med = max(50, K, int(0.5 / max(ms_graph / K / 1e3, 1e-6)) + 1)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_med + 1)]
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        evs[0].record(stream)
+        for i in range(n_med):
+            g.replay()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        windows.append((wall0, time.time()))
+        replay_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n_med)]
+        assert int(st.dev_status.item()) == 0
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(windows)
     ms = ms_graph if ms_graph is not None else ms_eager
 
     # end to end: every step's inputs come from pinned host memory and its result goes back
     # to pinned host memory, as in a serving loop: the copies run on a second stream through
     # double-buffered device staging, so step k+1's inputs and step k-1's result move while
     # step k computes; every step still carries its own copies.
-    # h, q_c and q_r are views of one contiguous device buffer (st.inputs): one copy each way
-    in_host = st.inputs.cpu().pin_memory()
+    # h, q_c and q_r are views of one contiguous device buffer (st.inputs): one copy each
+    # way; a workload that projects its query from h moves only h
+    dev_in = st.h.view(-1) if wl.query_from_h else st.inputs
+    in_host = dev_in.cpu().pin_memory()
     h2d = in_host.numel() * in_host.element_size()
     d2h = st.out.numel() * st.out.element_size()
     NS = 2
     copy_stream = torch.cuda.Stream()
-    stage_in = [torch.empty_like(st.inputs) for _ in range(NS)]
+    stage_in = [torch.empty_like(dev_in) for _ in range(NS)]
     stage_out = [torch.empty_like(st.out) for _ in range(NS)]
     out_host = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(NS)]
     ev_in = [torch.cuda.Event() for _ in range(NS)]      # inputs of the slot are on the device
@@ -331,7 +474,7 @@ def run_ours(args, wl, rank, world):
     def compute(k):
         sl = k % NS
         stream.wait_event(ev_in[sl])
-        st.inputs.copy_(stage_in[sl])
+        dev_in.copy_(stage_in[sl])
         if wl.query_from_h:
             st.x_q.copy_(st.h[:, -1, :])
         if g is not None:
@@ -390,10 +533,14 @@ def run_ours(args, wl, rank, world):
                                        "num_splits": args.num_splits or "auto",
                                        "launch": "cuda_graph" if ms_graph is not None else "eager"}),
         "ms_per_step_eager": ms_eager / K,
+        "ms_per_step_median": statistics.median(replay_ms) if replay_ms else None,
+        "ms_per_step_replays": len(replay_ms),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "traffic": ncu_traffic(wl.name), "kernel": DOMINANT_KERNEL_NAME,
                      "peak_source": f"{src} copy bandwidth",
-                     "algorithmic_bytes_per_launch": cache_bytes, "kernel_ms": split_ms},
+                     "frac_of_nominal": gbs / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": cache_bytes, "kernel_ms": split_ms,
+                     "kernel_ms_median": statistics.median(split_times)},
         "roofline_tensor": {"achieved": tfs, "unit": "TFLOP/s", "peak_burst": tf_burst,
                             "peak_sustained": tf_sus, "frac_burst": tfs / tf_burst,
                             "frac_sustained": tfs / tf_sus, "algorithmic_flops_per_launch": flops},
@@ -404,6 +551,9 @@ def run_ours(args, wl, rank, world):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if wl.name in FROM_H and not args.no_from_h and not args.no_graph:
+        line["h_to_o"] = time_from_h(args, FROM_H[wl.name])
+        line["output_projection"] = time_output_forms(args, wl.name)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
     return line

@@ -20,7 +20,10 @@ MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
             "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",
             "mla_profile_events", "mla_append_workspace_size", "mla_decode_absorbed_noalloc",
-            "mla_decode_prepare", "mla_decode_attend")
+            "mla_decode_prepare", "mla_decode_attend", "mla_set_wait_limit_ns",
+            "mla_project_query_latent", "mla_query_latent_workspace_size",
+            "mla_decode_absorbed_multi", "mla_decode_multi_workspace_size", "mla_project_output",
+            "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size")
 
 
 class MlaDims(ctypes.Structure):
@@ -53,12 +56,29 @@ def load():
     lib.mla_append_workspace_size.argtypes = [D, I32, I32, I32]
     lib.mla_append_workspace_size.restype = SZ
     lib.mla_cache_append.restype = I32
-    lib.mla_project_query.argtypes = [D, I32, I32, I32, P, P, P, P, P, P]
+    lib.mla_project_query.argtypes = [D, I32, I32, I32, P, P, P, P, P, P, P]
     lib.mla_project_query.restype = I32
+    lib.mla_project_query_latent.argtypes = [D, I32, I32, I32, P, P, P, SZ, P, P, P]
+    lib.mla_project_query_latent.restype = I32
+    lib.mla_query_latent_workspace_size.argtypes = [D, I32, I32, I32]
+    lib.mla_query_latent_workspace_size.restype = SZ
     lib.mla_decode_workspace_size.argtypes = [D, I32, I32, I32, I32]
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_absorbed.argtypes = [D, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
     lib.mla_decode_absorbed.restype = I32
+    lib.mla_decode_absorbed_multi.argtypes = [D, I32, I32, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P,
+                                              P]
+    lib.mla_decode_absorbed_multi.restype = I32
+    lib.mla_decode_multi_workspace_size.argtypes = [D, I32, I32, I32, I32, I32]
+    lib.mla_decode_multi_workspace_size.restype = SZ
+    lib.mla_project_output.argtypes = [D, I32, I32, P, P, P, SZ, P, P, P]
+    lib.mla_project_output.restype = I32
+    lib.mla_project_output_merged.argtypes = [D, I32, I32, P, P, P, SZ, P, P, P]
+    lib.mla_project_output_merged.restype = I32
+    lib.mla_merge_output_weights.argtypes = [D, I32, P, P, P, P, P]
+    lib.mla_merge_output_weights.restype = I32
+    lib.mla_output_workspace_size.argtypes = [D, I32, I32, I32]
+    lib.mla_output_workspace_size.restype = SZ
     for name in ("mla_decode_prepare", "mla_decode_attend"):
         getattr(lib, name).argtypes = lib.mla_decode_absorbed.argtypes
         getattr(lib, name).restype = I32
@@ -72,6 +92,8 @@ def load():
     lib.mla_launch_count.restype = ctypes.c_uint64
     lib.mla_profile_events.argtypes = [P, P]
     lib.mla_profile_events.restype = I32
+    lib.mla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.mla_set_wait_limit_ns.restype = ctypes.c_uint64
     _lib = lib
     return lib
 
@@ -121,10 +143,21 @@ def mla_cache_append(dims, dtype, batch, n_new, h, w_dkv, w_kr, row_off, cap, po
         _stream(stream)))
 
 
-def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, stream=None):
+def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, dev_status, stream=None):
     _check("mla_project_query", load().mla_project_query(
         ctypes.byref(dims), dtype, batch, d_in, _p(x), _p(w_uq), _p(w_qr), _p(q_c), _p(q_r),
-        _stream(stream)))
+        _p(dev_status), _stream(stream)))
+
+
+def mla_query_latent_workspace_size(dims, dtype, batch, d_q) -> int:
+    return int(load().mla_query_latent_workspace_size(ctypes.byref(dims), dtype, batch, d_q))
+
+
+def mla_project_query_latent(dims, dtype, batch, d_q, h, w_dq, workspace, workspace_bytes, c_q,
+                             dev_status, stream=None):
+    _check("mla_project_query_latent", load().mla_project_query_latent(
+        ctypes.byref(dims), dtype, batch, d_q, _p(h), _p(w_dq), _p(workspace), workspace_bytes, _p(c_q),
+        _p(dev_status), _stream(stream)))
 
 
 def mla_decode_workspace_size(dims, dtype, batch, max_seq_len, num_splits=0) -> int:
@@ -137,6 +170,21 @@ def mla_decode_absorbed(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, r
                         stream=None):
     _check("mla_decode_absorbed", load().mla_decode_absorbed(
         ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
+        _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
+
+
+def mla_decode_multi_workspace_size(dims, dtype, batch, n_q, max_seq_len, num_splits=0) -> int:
+    return int(load().mla_decode_multi_workspace_size(ctypes.byref(dims), dtype, batch, n_q, max_seq_len,
+                                                      num_splits))
+
+
+def mla_decode_absorbed_multi(dims, dtype, batch, n_q, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len,
+                              max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                              stream=None):
+    """n_q causal queries per sequence (query j at position seq_len[b] - n_q + j)."""
+    _check("mla_decode_absorbed_multi", load().mla_decode_absorbed_multi(
+        ctypes.byref(dims), dtype, batch, n_q, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
         _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
         _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
 
@@ -187,3 +235,33 @@ def mla_profile_events(start, stop):
             return e
         return e.cuda_event
     _check("mla_profile_events", load().mla_profile_events(h(start), h(stop)))
+
+
+def mla_set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' bounded waits for later launches (0 = default 2 s); returns the old one."""
+    return int(load().mla_set_wait_limit_ns(int(ns)))
+
+
+def mla_output_workspace_size(dims, dtype, batch, merged) -> int:
+    return int(load().mla_output_workspace_size(ctypes.byref(dims), dtype, batch, 1 if merged else 0))
+
+
+def mla_project_output(dims, dtype, batch, o, w_o, workspace, workspace_bytes, u, dev_status, stream=None):
+    """u = W_O [o_1; ...; o_n_h]."""
+    _check("mla_project_output", load().mla_project_output(
+        ctypes.byref(dims), dtype, batch, _p(o), _p(w_o), _p(workspace), workspace_bytes, _p(u),
+        _p(dev_status), _stream(stream)))
+
+
+def mla_merge_output_weights(dims, dtype, w_o, w_uv, w_ov, dev_status, stream=None):
+    """W_OV^(i) = W_O^(i) W_UV^(i), stored [n_h, d_c, hidden]."""
+    _check("mla_merge_output_weights", load().mla_merge_output_weights(
+        ctypes.byref(dims), dtype, _p(w_o), _p(w_uv), _p(w_ov), _p(dev_status), _stream(stream)))
+
+
+def mla_project_output_merged(dims, dtype, batch, o_lat, w_ov, workspace, workspace_bytes, u, dev_status,
+                              stream=None):
+    """u = sum_i W_OV^(i) o_lat_i."""
+    _check("mla_project_output_merged", load().mla_project_output_merged(
+        ctypes.byref(dims), dtype, batch, _p(o_lat), _p(w_ov), _p(workspace), workspace_bytes, _p(u),
+        _p(dev_status), _stream(stream)))

@@ -13,6 +13,8 @@ using namespace mla;
 namespace {
 
 std::atomic<unsigned long long> g_launches{0};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 thread_local cudaEvent_t t_ev_start = nullptr;
 thread_local cudaEvent_t t_ev_stop = nullptr;
 
@@ -21,6 +23,8 @@ thread_local cudaEvent_t t_ev_stop = nullptr;
 namespace mla {
 
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 void profile_before_split(cudaStream_t s) {
     if (t_ev_start) cudaEventRecord(t_ev_start, s);
@@ -135,6 +139,10 @@ const char* mla_status_string(mla_status s) {
 
 uint64_t mla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t mla_set_wait_limit_ns(uint64_t ns) {
+    return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
+
 mla_status mla_profile_events(void* start, void* stop) {
     if ((start == nullptr) != (stop == nullptr)) return MLA_ERR_INVALID_ARG;
     t_ev_start = (cudaEvent_t)start;
@@ -175,12 +183,98 @@ mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch
 
 mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
                              const void* x, const void* w_uq, const void* w_qr, void* q_c,
-                             void* q_r, void* stream) {
+                             void* q_r, int32_t* dev_status, void* stream) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || d_in < 1) return MLA_ERR_INVALID_ARG;
-    if (!x || !w_uq || !w_qr || !q_c || !q_r) return MLA_ERR_INVALID_ARG;
+    if (!x || !w_uq || !w_qr || !q_c || !q_r || !dev_status) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t m1 = (int64_t)dims->n_heads * dims->d_h, m2 = (int64_t)dims->n_heads * dims->d_r;
+    if (dtype == MLA_BF16 && m1 % 128 == 0 && m2 % 8 == 0 && m1 + m2 <= (1 << 24) && d_in % 64 == 0 &&
+        aligned(x, 16) && aligned(w_uq, 16) && aligned(w_qr, 16) && aligned(q_c, 16) && aligned(q_r, 16))
+        return cuda_status(launch_project_query_tc(*dims, batch, d_in, x, w_uq, w_qr, q_c, q_r, dev_status, s));
     return cuda_status(launch_project_query(*dims, dtype == MLA_BF16, batch, d_in, x, w_uq, w_qr,
-                                            q_c, q_r, (cudaStream_t)stream));
+                                            q_c, q_r, s));
+}
+
+// The output projection after the decode runs on tensor cores only: bf16 with d_h, d_c
+// and hidden multiples of 128.
+static bool output_tc(const mla_dims* d, mla_dtype t) {
+    return t == MLA_BF16 && d->d_h % 128 == 0 && d->d_c % 128 == 0 && d->hidden % 128 == 0 &&
+           (int64_t)d->n_heads * d->d_c <= (1 << 24);
+}
+
+size_t mla_output_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t merged) {
+    if (!dims_ok(dims) || !dtype_ok(dtype) || batch < 1 || !output_tc(dims, dtype)) return 0;
+    const int k_in = dims->n_heads * (merged ? dims->d_c : dims->d_h);
+    return output_tc_workspace(dims->hidden, k_in, batch, sm_count());
+}
+
+static mla_status output_common(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* x,
+                                const void* w, void* workspace, size_t workspace_bytes, void* u,
+                                int32_t* dev_status, bool merged) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || !x || !w || !u || !dev_status) return MLA_ERR_INVALID_ARG;
+    if (!output_tc(dims, dtype)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(u, 4)) return MLA_ERR_INVALID_ARG;
+    const size_t need = mla_output_workspace_size(dims, dtype, batch, merged ? 1 : 0);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    return MLA_OK;
+}
+
+mla_status mla_project_output(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o,
+                              const void* w_o, void* workspace, size_t workspace_bytes, void* u,
+                              int32_t* dev_status, void* stream) {
+    const mla_status st = output_common(dims, dtype, batch, o, w_o, workspace, workspace_bytes, u, dev_status, false);
+    if (st != MLA_OK) return st;
+    return cuda_status(launch_output_tc(*dims, batch, o, w_o, workspace, u, dev_status, sm_count(),
+                                        (cudaStream_t)stream));
+}
+
+mla_status mla_project_output_merged(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o_lat,
+                                     const void* w_ov, void* workspace, size_t workspace_bytes, void* u,
+                                     int32_t* dev_status, void* stream) {
+    const mla_status st = output_common(dims, dtype, batch, o_lat, w_ov, workspace, workspace_bytes, u, dev_status,
+                                        true);
+    if (st != MLA_OK) return st;
+    return cuda_status(launch_output_merged_tc(*dims, batch, o_lat, w_ov, workspace, u, dev_status, sm_count(),
+                                               (cudaStream_t)stream));
+}
+
+mla_status mla_merge_output_weights(const mla_dims* dims, mla_dtype dtype, const void* w_o, const void* w_uv,
+                                    void* w_ov, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (!w_o || !w_uv || !w_ov || !dev_status) return MLA_ERR_INVALID_ARG;
+    if (!output_tc(dims, dtype)) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(w_o, 16) || !aligned(w_uv, 16) || !aligned(w_ov, 16)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_merge_output_weights_tc(*dims, w_o, w_uv, w_ov, dev_status, (cudaStream_t)stream));
+}
+
+static bool query_latent_tc(const mla_dims* d, mla_dtype t, int32_t d_q) {
+    return t == MLA_BF16 && d_q % 128 == 0 && d->hidden % 64 == 0;
+}
+
+size_t mla_query_latent_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_q) {
+    if (!dims_ok(dims) || !dtype_ok(dtype) || batch < 1 || d_q < 1) return 0;
+    if (!query_latent_tc(dims, dtype, d_q)) return 0;
+    return query_latent_tc_workspace(dims->hidden, d_q, batch, nullptr, sm_count());
+}
+
+mla_status mla_project_query_latent(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_q,
+                                    const void* h, const void* w_dq, void* workspace, size_t workspace_bytes,
+                                    void* c_q, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || d_q < 1 || (int64_t)batch * d_q > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+    if (!h || !w_dq || !c_q || !dev_status) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (query_latent_tc(dims, dtype, d_q)) {
+        const int sms = sm_count();
+        const size_t need = query_latent_tc_workspace(dims->hidden, d_q, batch, nullptr, sms);
+        if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+        if (!aligned(h, 16) || !aligned(w_dq, 16) || !aligned(c_q, 4)) return MLA_ERR_INVALID_ARG;
+        return cuda_status(launch_query_latent_tc(dims->hidden, d_q, batch, h, w_dq, workspace, c_q,
+                                                  dev_status, sms, s));
+    }
+    return cuda_status(launch_query_latent(*dims, dtype == MLA_BF16, batch, d_q, h, w_dq, c_q, s));
 }
 
 size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
@@ -233,29 +327,37 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
     const bool bf16 = dtype == MLA_BF16;
     const float alpha = scale_of(dims) * kLog2e;
     cudaError_t e = cudaSuccess;
+    const ScheduleArgs sa{seq_len, row_off, cache_rows, batch, p.workers, cum, (Schedule*)sched, wstart,
+                          dev_status};
     if (phases & kPrepare) {
         if (tc && gemm_tc_shapes_ok(*dims) && aligned(q_c, 16) && aligned(w_uk, 16)) {
             // fold GEMM, then q_R rotation and the schedule in one launch
-            const ScheduleArgs sa{seq_len, row_off, cache_rows, batch, p.workers, cum, (Schedule*)sched, wstart,
-                                  dev_status};
+            // the rotation and schedule kernel runs beside the fold GEMM (programmatic
+            // dependent launch; it waits for the GEMM only at its end)
             e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s);
-            if (e == cudaSuccess) e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s, &sa);
+            if (e == cudaSuccess)
+                e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s, &sa, true);
         } else {
             e = launch_fold(*dims, bf16, tc, batch, q_c, q_r, w_uk, seq_len, alpha, qp, s);
-            if (e == cudaSuccess)
-                e = launch_schedule(seq_len, row_off, cache_rows, batch, p.workers, cum, sched, wstart, dev_status, s);
+            if (e == cudaSuccess) e = launch_schedule(sa, s);
         }
     }
     if (e == cudaSuccess && (phases & kAttend)) {
-        if (tc)
+        if (tc) {
+            // when this call also ran the prepare kernels, the attention kernel may start
+            // (set-up only) before the last of them ends
             e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cache, cache_rows, row_off, cum,
-                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s);
-        else
+                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s,
+                                (phases & kPrepare) != 0);
+        } else {
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
                                   sched, wstart, o_lat, lse, part_o, part_l, s);
+        }
+        // the merge kernel follows the attention kernel of this same call (programmatic
+        // dependent launch: it is scheduled early and waits for it)
+        if (e == cudaSuccess)
+            e = launch_merge(*dims, bf16, batch, cum, sched, part_o, part_l, o_lat, lse, s, true);
     }
-    if (e == cudaSuccess && (phases & kAttend))
-        e = launch_merge(*dims, bf16, batch, cum, sched, part_o, part_l, o_lat, lse, s);
     return cuda_status(e);
 }
 
@@ -272,6 +374,49 @@ mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, int32_t ba
     return decode_phases(kPrepare | kAttend, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
                          seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
                          stream);
+}
+
+// Several causal queries per sequence: query j of sequence b sits at position
+// seq_len[b] - n_q + j and attends over rows 0 .. that position.  Each query becomes a
+// sequence of its own for the decode (same cache rows, its own length), so the same
+// kernels run on batch * n_q sequences; the expanded row offsets and lengths sit at the
+// start of the workspace, the decode's own workspace after them.
+static size_t multi_index_bytes(int64_t n) {
+    return align_up((size_t)n * sizeof(int64_t), 256) + align_up((size_t)n * sizeof(int32_t), 256);
+}
+
+size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_q,
+                                       int32_t max_seq_len, int32_t num_splits) {
+    if (batch < 1 || n_q < 1 || (int64_t)batch * n_q > (1 << 30)) return 0;
+    const size_t dec = mla_decode_workspace_size(dims, dtype, batch * n_q, max_seq_len, num_splits);
+    return dec ? multi_index_bytes((int64_t)batch * n_q) + dec : 0;
+}
+
+mla_status mla_decode_absorbed_multi(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_q,
+                                     const void* q_c, const void* q_r, const void* w_uk,
+                                     const void* cache, int64_t cache_rows, const int64_t* row_off,
+                                     const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                                     void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                     int32_t* dev_status, void* stream) {
+    if (batch < 1 || n_q < 1 || (int64_t)batch * n_q > (1 << 30)) return MLA_ERR_INVALID_ARG;
+    if (!row_off || !seq_len || !dev_status) return MLA_ERR_INVALID_ARG;
+    const int64_t nv = (int64_t)batch * n_q;
+    const size_t idx = multi_index_bytes(nv);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < idx) return MLA_ERR_WORKSPACE;
+    int64_t* row_off_v = (int64_t*)workspace;
+    int32_t* seq_len_v = (int32_t*)((char*)workspace + align_up((size_t)nv * sizeof(int64_t), 256));
+    // host checks of the decode first (nothing is enqueued when they fail)
+    DecodePlan p;
+    if (!dims_ok(dims) || !dtype_ok(dtype) || max_seq_len < 0 || num_splits < 0) return MLA_ERR_INVALID_ARG;
+    if (!plan_decode(dims, dtype, (int)nv, max_seq_len, num_splits,
+                     tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX, &p))
+        return tc_shape(dims, dtype) || simt_supported(dims) ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+    if (workspace_bytes - idx < p.ws.total) return MLA_ERR_WORKSPACE;
+    cudaError_t e = launch_expand_queries(row_off, seq_len, batch, n_q, row_off_v, seq_len_v, (cudaStream_t)stream);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    return decode_phases(kPrepare | kAttend, dims, dtype, (int32_t)nv, q_c, q_r, w_uk, cache, cache_rows, row_off_v,
+                         seq_len_v, max_seq_len, num_splits, (char*)workspace + idx, workspace_bytes - idx, o_lat,
+                         lse, dev_status, stream);
 }
 
 mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t batch,

@@ -79,7 +79,21 @@ struct Schedule {
     int64_t per;        // rows per worker range (>= 1)
     int32_t workers;
     int32_t batch;
+    int32_t whole;      // 1: worker g takes sequence g whole (no sequence is cut)
 };
+
+// Rows [*begin, *end) of the flattened context that worker g covers: an equal share
+// (the last one shorter), or sequence g whole.
+__host__ __device__ __forceinline__ void worker_range(const Schedule& S, const int64_t* cum, int g,
+                                                      int64_t* begin, int64_t* end) {
+    if (S.whole) {
+        *begin = g < S.batch ? cum[g] : 0;
+        *end = g < S.batch ? cum[g + 1] : 0;
+    } else {
+        *begin = (int64_t)g * S.per;
+        *end = *begin + S.per < S.total ? *begin + S.per : S.total;
+    }
+}
 
 // Layout of the decode workspace (offsets in bytes, each 256-aligned).
 struct DecodeWorkspace {
@@ -93,5 +107,31 @@ struct DecodeWorkspace {
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- programmatic dependent launch --------------------------------------------------
+// A kernel launched with pdl = true may start while the previous kernel of its stream
+// (always one of this library's, enqueued by the same call) is still running.  It must
+// call pdl_wait() before it touches memory that kernel writes or reads; pdl_wait()
+// returns once that kernel has completed and its writes are visible (and at once for a
+// kernel launched without the attribute).  pdl_trigger() lets the next such kernel be
+// scheduled before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? at : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace mla

@@ -18,6 +18,20 @@ namespace {
 // ------------------------------------------------------------------ schedule
 __global__ void __launch_bounds__(1024) schedule_kernel(ScheduleArgs a) { build_schedule(a); }
 
+// ------------------------------------------------------------------ multi-query index
+__global__ void __launch_bounds__(256) expand_queries_kernel(const int64_t* __restrict__ row_off,
+                                                             const int32_t* __restrict__ seq_len, int batch,
+                                                             int n_q, int64_t* __restrict__ row_off_v,
+                                                             int32_t* __restrict__ seq_len_v) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)batch * n_q) return;
+    const int64_t b = i / n_q, j = i % n_q;
+    row_off_v[i] = row_off[b];
+    // a length below 1 marks the query as empty (flagged and zero-filled by the decode)
+    const int64_t len = (int64_t)seq_len[b] - n_q + j + 1;
+    seq_len_v[i] = (int32_t)(len < 0 ? 0 : len);
+}
+
 // ------------------------------------------------------------------ SIMT split
 constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
 
@@ -36,8 +50,8 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
     float* qs = smem + kTileRows * ts;          // [kWarps][dq]
     const Schedule S = *a.sched;
     const int g = blockIdx.x;
-    const int64_t begin = (int64_t)g * S.per;
-    const int64_t end = min(begin + S.per, S.total);
+    int64_t begin, end;
+    worker_range(S, a.cum, g, &begin, &end);
     if (begin >= end) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y * kWarps + warp;
@@ -147,6 +161,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
                                                                  const float* __restrict__ part_l,
                                                                  Tout* __restrict__ o_lat,
                                                                  float* __restrict__ lse, int n_h, int d_c) {
+    pdl_wait();                                 // launched behind the split kernel
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31;
     const int h = blockIdx.y * kMergeHeads + (threadIdx.x >> 5);
@@ -159,6 +174,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
         if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = -INFINITY;
         return;
     }
+    if (sched->whole) return;                   // every sequence was finished by its worker
     const int64_t first_w = seq0 / per, last_w = (seq1 - 1) / per;
     if (first_w == last_w) return;              // finished in place by its only worker
     const int64_t np = last_w - first_w + 1;
@@ -211,11 +227,42 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
                     if (e < nc) acc[e] = fmaf(wp, src[e], acc[e]);
             }
         };
+        if (vec && nc == kCols) {
+            // four pieces per round: sixteen 16-byte loads of a lane in flight together
 #pragma unroll
-        for (int k = 0; k < kMergeRegs; ++k) {
-            if (32 * k >= np) break;
-            const int nj = (int)min((int64_t)32, np - 32 * k);
-            for (int j = 0; j < nj; ++j) add_piece(32 * k + j, __shfl_sync(0xffffffffu, lr[k], j));
+            for (int k = 0; k < kMergeRegs; ++k) {
+                if (32 * k >= np) break;
+                const int nj = (int)min((int64_t)32, np - 32 * k);
+                for (int j0 = 0; j0 < nj; j0 += 4) {
+                    float4 v[4][kCols / 4];
+                    float wp[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = j0 + u < nj ? j0 + u : j0;
+                        wp[u] = j0 + u < nj ? exp2f(__shfl_sync(0xffffffffu, lr[k], j) - mx) * inv : 0.f;
+                        const float4* src = reinterpret_cast<const float4*>(
+                            part_o + (piece_slot(first_w + 32 * k + j, seq0, per) * n_h + h) * d_c + c0);
+#pragma unroll
+                        for (int q = 0; q < kCols / 4; ++q) v[u][q] = src[q];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int q = 0; q < kCols / 4; ++q) {
+                            acc[4 * q] = fmaf(wp[u], v[u][q].x, acc[4 * q]);
+                            acc[4 * q + 1] = fmaf(wp[u], v[u][q].y, acc[4 * q + 1]);
+                            acc[4 * q + 2] = fmaf(wp[u], v[u][q].z, acc[4 * q + 2]);
+                            acc[4 * q + 3] = fmaf(wp[u], v[u][q].w, acc[4 * q + 3]);
+                        }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kMergeRegs; ++k) {
+                if (32 * k >= np) break;
+                const int nj = (int)min((int64_t)32, np - 32 * k);
+                for (int j = 0; j < nj; ++j) add_piece(32 * k + j, __shfl_sync(0xffffffffu, lr[k], j));
+            }
         }
         for (int64_t p = 32 * kMergeRegs; p < np; ++p)
             add_piece(p, part_l[piece_slot(first_w + p, seq0, per) * n_h + h]);
@@ -227,10 +274,16 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
 
 }  // namespace
 
-cudaError_t launch_schedule(const int32_t* seq_len, const int64_t* row_off, int64_t cache_rows,
-                            int batch, int workers, int64_t* cum, void* sched, int32_t* wstart,
-                            int32_t* dev_status, cudaStream_t s) {
-    ScheduleArgs a{seq_len, row_off, cache_rows, batch, workers, cum, (Schedule*)sched, wstart, dev_status};
+cudaError_t launch_expand_queries(const int64_t* row_off, const int32_t* seq_len, int batch, int n_q,
+                                  int64_t* row_off_v, int32_t* seq_len_v, cudaStream_t s) {
+    const int64_t n = (int64_t)batch * n_q;
+    expand_queries_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(row_off, seq_len, batch, n_q, row_off_v,
+                                                                      seq_len_v);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const ScheduleArgs& a, cudaStream_t s) {
     schedule_kernel<<<1, 1024, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
@@ -276,16 +329,17 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
 
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
                          const void* sched, const float* part_o, const float* part_l, void* o_lat,
-                         float* lse, cudaStream_t s) {
+                         float* lse, cudaStream_t s, bool pdl) {
     const dim3 grid(batch, (d.n_heads + kMergeHeads - 1) / kMergeHeads);
+    cudaError_t e;
     if (bf16)
-        merge_kernel<<<grid, 32 * kMergeHeads, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                                       (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
+        e = launch_ex(merge_kernel<__nv_bfloat16>, grid, dim3(32 * kMergeHeads), 0, s, pdl, cum,
+                      (const Schedule*)sched, part_o, part_l, (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
     else
-        merge_kernel<<<grid, 32 * kMergeHeads, 0, s>>>(cum, (const Schedule*)sched, part_o, part_l,
-                                                       (float*)o_lat, lse, d.n_heads, d.d_c);
+        e = launch_ex(merge_kernel<float>, grid, dim3(32 * kMergeHeads), 0, s, pdl, cum, (const Schedule*)sched,
+                      part_o, part_l, (float*)o_lat, lse, d.n_heads, d.d_c);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

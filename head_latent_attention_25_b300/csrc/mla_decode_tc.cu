@@ -51,7 +51,7 @@ constexpr int kHeads = 128;           // MMA M (heads beyond n_heads are compute
 constexpr int kLatHalf = 256;         // latent columns per CTA
 constexpr int kRopeHalf = 32;         // rotary columns per CTA
 constexpr int kRowElems = 576;        // d_c + d_r
-constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // bound of the drain waits after an abort
 
 // shared memory layout (byte offsets from a 1024-aligned base)
 constexpr uint32_t kTBox = kTok * 128;                   // 64 rows x 64 bf16, 128B swizzle
@@ -101,6 +101,7 @@ struct TcArgs {
     float* part_o;
     float* part_l;
     int32_t* dev_status;
+    uint64_t wait_ns;                  // limit of every wait of the pipeline
     int n_h;
     int batch;
 };
@@ -112,19 +113,18 @@ struct Seg {
     int64_t slot;
 };
 
-// Walks the sequences that a worker's range [g*per, (g+1)*per) of the flattened
-// context touches (identical in every role of both CTAs).
+// Walks the sequences that a worker's range of the flattened context touches
+// (identical in every role of both CTAs).
 struct SegWalk {
     const int64_t* cum;
     int64_t cur, end;
     int b, g;
     bool first;
     // start: the worker's first sequence, found by the schedule kernel
-    __device__ void init(const int64_t* c, int start, int gi, int64_t per, int64_t total) {
+    __device__ void init(const int64_t* c, int start, int gi, const Schedule& S) {
         cum = c;
         g = gi;
-        cur = (int64_t)gi * per;
-        end = min(cur + per, total);
+        worker_range(S, c, gi, &cur, &end);
         first = true;
         b = start;
     }
@@ -171,6 +171,7 @@ struct TileIt {
 struct Ctl {
     volatile int* abort;
     int32_t* dev_status;
+    uint64_t limit_ns;
 };
 
 // Bounded wait: true when the phase completed; false on abort or time-out (which
@@ -182,7 +183,7 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c
     while (true) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
+        if (globaltimer_ns() - t0 > c.limit_ns) {
             *c.abort = 1;
             atomicOr(c.dev_status, MLA_DEV_TIMEOUT);
             return false;
@@ -222,10 +223,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const Schedule S = *a.sched;
-    const int g = blockIdx.x >> 1;
-    if ((int64_t)g * S.per >= S.total) return;          // both CTAs of the pair leave together
-
     const uint32_t base = smem_addr(sm);
     const uint32_t sStage = base + kOffStage, sX = base + kOffX;
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
@@ -236,7 +233,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    Ctl ctl{abort_flag, a.dev_status};
+    Ctl ctl{abort_flag, a.dev_status, a.wait_ns};
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
@@ -274,391 +271,402 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     cluster_sync();                 // barriers of both CTAs initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // Everything above touches only this CTA's shared and tensor memory.  Everything below
+    // reads what the kernels before this one wrote: launched behind them (programmatic
+    // dependent launch), the kernel waits here, so its set-up overlaps their tail.
+    pdl_wait();
+    pdl_trigger();                  // the merge kernel behind this one may be scheduled
+    const Schedule S = *a.sched;
+    const int g = blockIdx.x >> 1;
+    int64_t r_begin, r_end;
+    worker_range(S, a.cum, g, &r_begin, &r_end);
+    const bool active = r_begin < r_end;               // the same for both CTAs of the pair
 
     // Registers: 128 per thread at launch; each role re-sizes its warpgroup's share
     // first thing in its own branch (80 + 168 + 168 + 96 = 4 x 128).
-    if (warp < 4) reg_alloc_dec<80>();
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer + credits
-        // One thread serves two queues in an event loop: TMA loads of cache tiles into
-        // the ring, and the return of exchange buffers to the peer (a group that has read
-        // the peer's partial arrives on a local barrier; this thread, which has no remote
-        // stores of its own in flight, makes the cluster-scope release arrival).
-        if (lane == 0) {
-            TileIt ip, ic;                              // next tile to load, next credit
-            ip.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-            ic.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-            bool mp = ip.next(), mc = ic.next();
-            uint32_t issued = 0;
-            uint64_t t_prog = globaltimer_ns();
-            while (mp || mc) {
-                bool prog = false;
-                if (mp) {
-                    const uint32_t T = ip.T, st = T % kStages;
-                    if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
-                        const uint32_t dst = sStage + st * kStageBytes;
-                        const int y = (int)(a.row_off[ip.seg.b] + ip.seg.lo + (int64_t)ip.t * kTok);
-                        mbar_expect_tx(bar(B_FULL + st), kStageBytes);
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
-                        tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
-                        issued = T + 1;
-                        mp = ip.next();
-                        prog = true;
+    if (active) {
+        if (warp < 4) reg_alloc_dec<80>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer + credits
+            // One thread serves two queues in an event loop: TMA loads of cache tiles into
+            // the ring, and the return of exchange buffers to the peer (a group that has read
+            // the peer's partial arrives on a local barrier; this thread, which has no remote
+            // stores of its own in flight, makes the cluster-scope release arrival).
+            if (lane == 0) {
+                TileIt ip, ic;                              // next tile to load, next credit
+                ip.walk.init(a.cum, a.wstart[g], g, S);
+                ic.walk.init(a.cum, a.wstart[g], g, S);
+                bool mp = ip.next(), mc = ic.next();
+                uint32_t issued = 0;
+                uint64_t t_prog = globaltimer_ns();
+                while (mp || mc) {
+                    bool prog = false;
+                    if (mp) {
+                        const uint32_t T = ip.T, st = T % kStages;
+                        if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
+                            const uint32_t dst = sStage + st * kStageBytes;
+                            const int y = (int)(a.row_off[ip.seg.b] + ip.seg.lo + (int64_t)ip.t * kTok);
+                            mbar_expect_tx(bar(B_FULL + st), kStageBytes);
+                            for (int j = 0; j < 4; ++j)
+                                tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
+                            tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
+                            issued = T + 1;
+                            mp = ip.next();
+                            prog = true;
+                        }
+                    }
+                    if (mc) {
+                        const uint32_t T = ic.T;
+                        if (mbar_test_wait_cluster(bar(B_XCONS + (T & 1)), (T >> 1) & 1)) {
+                            mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
+                            mc = ic.next();
+                            prog = true;
+                        }
+                    }
+                    if (prog) {
+                        t_prog = globaltimer_ns();
+                    } else {
+                        if (*abort_flag) break;
+                        if (globaltimer_ns() - t_prog > a.wait_ns) {
+                            *abort_flag = 1;
+                            atomicOr(a.dev_status, MLA_DEV_TIMEOUT);
+                            break;
+                        }
                     }
                 }
-                if (mc) {
-                    const uint32_t T = ic.T;
-                    if (mbar_test_wait_cluster(bar(B_XCONS + (T & 1)), (T >> 1) & 1)) {
-                        mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
-                        mc = ic.next();
-                        prog = true;
-                    }
-                }
-                if (prog) {
-                    t_prog = globaltimer_ns();
-                } else {
-                    if (*abort_flag) break;
-                    if (globaltimer_ns() - t_prog > kTimeoutNs) {
-                        *abort_flag = 1;
-                        atomicOr(a.dev_status, MLA_DEV_TIMEOUT);
-                        break;
-                    }
+                // drain: every copy this thread issued has landed before the CTA may exit
+                for (uint32_t k = 0; k < kStages && k < issued; ++k) {
+                    const uint32_t Tk = issued - 1 - k;
+                    drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
                 }
             }
-            // drain: every copy this thread issued has landed before the CTA may exit
-            for (uint32_t k = 0; k < kStages && k < issued; ++k) {
-                const uint32_t Tk = issued - 1 - k;
-                drain(bar(B_FULL + Tk % kStages), (Tk / kStages) & 1);
+        } else if (warp == 1 || warp == 3) {
+            // ------------------------------------------------------------ score MMA issuers
+            // Warp 1 issues the score MMAs of the even tiles into S[0], warp 3 those of the odd
+            // tiles into S[1]: two issue streams, so a score never waits for the previous
+            // tile's scores to be read.  With an even ring depth each stage, and so each
+            // FULL barrier, belongs to one issuer.  Both wait for every piece's Q' and both
+            // release it (QEMPTY counts two commits).
+            if (lane == 0) {
+                const uint32_t par = warp == 1 ? 0u : 1u;
+                const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
+                const uint32_t sQR = base + kOffQR;
+                TileIt it;
+                it.walk.init(a.cum, a.wstart[g], g, S);
+                bool ok = true;
+                while (ok && it.next()) {
+                    const uint32_t T = it.T;
+                    if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
+                    if ((T & 1u) == par) {
+                        const uint32_t st = T % kStages;
+                        if (!(ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl))) break;
+                        if (T >= 2 && !(ok = wait<false>(bar(B_SEMPTY + par), ((T >> 1) - 1) & 1, ctl))) break;
+                        tc_fence_after();
+                        const uint32_t stage = sStage + st * kStageBytes;
+                        const uint32_t d = tmem + kColS + 64 * par;
+                        for (int kk = 0; kk < 16; ++kk)
+                            mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
+                                        id_s, kk ? 1u : 0u);
+                        for (int kk = 0; kk < 2; ++kk)
+                            mma_bf16(d, kdesc64(sQR + 32 * kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
+                        mma_commit(bar(B_SFULL + par));
+                    }
+                    if (it.last_tile()) mma_commit(bar(B_QEMPTY));
+                }
+                mma_commit(bar(B_FIN));
+                drain(bar(B_FIN), 0);
             }
-        }
-    } else if (warp == 1 || warp == 3) {
-        // ------------------------------------------------------------ score MMA issuers
-        // Warp 1 issues the score MMAs of the even tiles into S[0], warp 3 those of the odd
-        // tiles into S[1]: two issue streams, so a score never waits for the previous
-        // tile's scores to be read.  With an even ring depth each stage, and so each
-        // FULL barrier, belongs to one issuer.  Both wait for every piece's Q' and both
-        // release it (QEMPTY counts two commits).
-        if (lane == 0) {
-            const uint32_t par = warp == 1 ? 0u : 1u;
-            const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
-            const uint32_t sQR = base + kOffQR;
-            TileIt it;
-            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-            bool ok = true;
-            while (ok && it.next()) {
-                const uint32_t T = it.T;
-                if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
-                if ((T & 1u) == par) {
-                    const uint32_t st = T % kStages;
-                    if (!(ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl))) break;
-                    if (T >= 2 && !(ok = wait<false>(bar(B_SEMPTY + par), ((T >> 1) - 1) & 1, ctl))) break;
+        } else if (warp == 2) {
+            // ------------------------------------------------------------ value MMA issuer
+            // O_r += P C_r: P (bf16, 128 heads x 64 rows) from shared memory, the tile's
+            // latent half as an MN-major B operand.  A stage is released here: the value MMA
+            // of a tile always completes after its score MMA (the softmax in between needs it).
+            if (lane == 0) {
+                const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
+                const uint32_t sP = base + kOffP;
+                TileIt it;
+                it.walk.init(a.cum, a.wstart[g], g, S);
+                bool ok = true;
+                while (ok && it.next()) {
+                    const uint32_t T = it.T, st = T % kStages;
+                    if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
+                    if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
                     tc_fence_after();
                     const uint32_t stage = sStage + st * kStageBytes;
-                    const uint32_t d = tmem + kColS + 64 * par;
-                    for (int kk = 0; kk < 16; ++kk)
-                        mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
-                                    id_s, kk ? 1u : 0u);
-                    for (int kk = 0; kk < 2; ++kk)
-                        mma_bf16(d, kdesc64(sQR + 32 * kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
-                    mma_commit(bar(B_SFULL + par));
+                    for (int k = 0; k < kTok / 16; ++k)
+                        mma_bf16(tmem + kColO, kdesc128(sP + 32 * k), mndesc128(stage + 2048 * k), id_o,
+                                 (it.first_tile() && k == 0) ? 0u : 1u);
+                    mma_commit(bar(B_EMPTY + st));
+                    mma_commit(bar(B_VDONE + (T & 1)));
                 }
-                if (it.last_tile()) mma_commit(bar(B_QEMPTY));
+                // every MMA this thread issued has completed before the CTA may tear down
+                mma_commit(bar(B_FIN));
+                drain(bar(B_FIN), 0);
             }
-            mma_commit(bar(B_FIN));
-            drain(bar(B_FIN), 0);
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ value MMA issuer
-        // O_r += P C_r: P (bf16, 128 heads x 64 rows) from shared memory, the tile's
-        // latent half as an MN-major B operand.  A stage is released here: the value MMA
-        // of a tile always completes after its score MMA (the softmax in between needs it).
-        if (lane == 0) {
-            const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
-            const uint32_t sP = base + kOffP;
-            TileIt it;
-            it.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
+        } else if (warp >= 4 && warp < 12) {
+            // ------------------------------------------------------------ softmax / exchange
+            reg_alloc_inc<168>();
+            // Two groups of four warps take alternate tiles (group grp owns the tiles T with
+            // T % 2 == grp), so one group's exchange overlaps the other's exponentials.  The
+            // running maximum is handed from the owner of tile T-1 to the owner of tile T
+            // through shared memory; each group keeps its own sum relative to the maximum it
+            // last saw, and the epilogue combines the two.
+            const int grp = (warp - 4) >> 2;
+            const int i = (tid - 128) & (kHeads - 1);      // head row == TMEM lane
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t xb = (uint32_t)grp;              // this group's exchange buffer
+            const uint32_t peer_x = mapa(sX + xb * kXBytes, peer);
+            const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
+                float* mshare = (float*)(sm + kOffMh);
+            TileIt co;
+            co.walk.init(a.cum, a.wstart[g], g, S);
             bool ok = true;
-            while (ok && it.next()) {
-                const uint32_t T = it.T, st = T % kStages;
-                if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
-                if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
-                tc_fence_after();
-                const uint32_t stage = sStage + st * kStageBytes;
-                for (int k = 0; k < kTok / 16; ++k)
-                    mma_bf16(tmem + kColO, kdesc128(sP + 32 * k), mndesc128(stage + 2048 * k), id_o,
-                             (it.first_tile() && k == 0) ? 0u : 1u);
-                mma_commit(bar(B_EMPTY + st));
-                mma_commit(bar(B_VDONE + (T & 1)));
-            }
-            // every MMA this thread issued has completed before the CTA may tear down
-            mma_commit(bar(B_FIN));
-            drain(bar(B_FIN), 0);
-        }
-    } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------------------ softmax / exchange
-        reg_alloc_inc<168>();
-        // Two groups of four warps take alternate tiles (group grp owns the tiles T with
-        // T % 2 == grp), so one group's exchange overlaps the other's exponentials.  The
-        // running maximum is handed from the owner of tile T-1 to the owner of tile T
-        // through shared memory; each group keeps its own sum relative to the maximum it
-        // last saw, and the epilogue combines the two.
-        const int grp = (warp - 4) >> 2;
-        const int i = (tid - 128) & (kHeads - 1);      // head row == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t xb = (uint32_t)grp;              // this group's exchange buffer
-        const uint32_t peer_x = mapa(sX + xb * kXBytes, peer);
-        const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
-            float* mshare = (float*)(sm + kOffMh);
-        TileIt co;
-        co.walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-        bool ok = true;
-        float m_g = -INFINITY, l_g = 0.f;
-        while (ok && co.next()) {
-            const uint32_t T = co.T;
-            if (co.first_tile()) { m_g = -INFINITY; l_g = 0.f; }
-            if ((T & 1u) == xb) {
-                const uint32_t st = T % kStages;
-                // this CTA's partial scores: out of TMEM, then to the peer
-                float s[kTok];
-                if (!(ok = wwait<false>(bar(B_SFULL + xb), (T >> 1) & 1, ctl))) break;
-                tc_fence_after();
-                tmem_ld32(tmem + lane_base + kColS + 64 * xb, *reinterpret_cast<float(*)[32]>(&s[0]));
-                tmem_ld32(tmem + lane_base + kColS + 64 * xb + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar(B_SEMPTY + xb));
-                // the peer has finished reading what this group sent for tile T - 2
-                if (T >= 2 && !(ok = wwait<true>(bar(B_XEMPTY + xb), ((T >> 1) - 1) & 1, ctl))) break;
-                if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
-                {
-                    // block-scaled fp16: s = off + r with off the partial of the tile's first
-                    // row (always a row of the piece), so each r is rounded relative to the
-                    // spread of the partial within the tile, not to its magnitude
-                    // (|error| <= 2^-11 |s - off|)
-                    const float off = s[0];
-#pragma unroll
-                    for (int c = 0; c < kTok / 8; ++c) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __half2 h2 = __floats2half2_rn(s[8 * c + 2 * e] - off, s[8 * c + 2 * e + 1] - off);
-                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                        }
-                        st_async_v4u(peer_x + (uint32_t)(c * kHeads + i) * 16, w[0], w[1], w[2], w[3], peer_xfull);
-                    }
-                    st_async_f32(peer_x + kXResBytes + (uint32_t)i * 4, off, peer_xfull);
-                }
-                // add the peer's partial scores of tile T
-                if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
-                {
-                    const uint8_t* xbase = sm + kOffX + xb * kXBytes;
-                    const uint4* xr = reinterpret_cast<const uint4*>(xbase) + i;
-                    const float off = reinterpret_cast<const float*>(xbase + kXResBytes)[i];
-#pragma unroll
-                    for (int c = 0; c < kTok / 8; ++c) {
-                        const uint4 v = xr[c * kHeads];
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                            s[8 * c + 2 * e] += f.x + off;
-                            s[8 * c + 2 * e + 1] += f.y + off;
-                        }
-                    }
-                }
-                mbar_arrive(bar(B_XCONS + xb));
-                // rows past the end of this piece do not count (only the last tile of a
-                // piece is partial)
-                const int valid = co.valid_rows();
-                if (valid < kTok) {
-#pragma unroll
-                    for (int j = 0; j < kTok; ++j)
-                        if (j >= valid) s[j] = -INFINITY;
-                }
-                // tile maximum: eight running maxima, then a tree (short dependency chains)
-                float m8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    m8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
-                                  fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
-#pragma unroll
-                for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-                    for (int j = 0; j < w; ++j) m8[j] = fmaxf(m8[j], m8[j + w]);
-                const float mt = m8[0];
-                // the running maximum after tile T - 1 (decided by the other group)
-                if (T > 0) {
-                    if (!(ok = wwait<false>(bar(B_MH + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
-                    const float mp = mshare[((T - 1) & 1) * kHeads + i];
-                    if (!co.first_tile() && mp != m_g) { l_g *= fast_exp2(m_g - mp); m_g = mp; }
-                }
-                // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
-                const bool need = mt > m_g + 8.f;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = fast_exp2(m_g - mt);
-                    m_g = mt;
-                    l_g *= alpha;
-                }
-                mshare[(T & 1) * kHeads + i] = m_g;
-                mbar_arrive(bar(B_MH + (T & 1)));
-                // P tile (bf16) for the value MMA; the sum uses the rounded values
-                uint32_t packed[kTok / 2];
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums (short chains)
-#pragma unroll
-                for (int j = 0; j < kTok / 2; ++j) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_g),
-                                                                    fast_exp2(s[2 * j + 1] - m_g));
-                    ls[j & 3] += __low2float(h2) + __high2float(h2);
-                    packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
-                l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                // the value MMA of the previous tile has finished with P and O
-                if (T > 0) {
-                    if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+            float m_g = -INFINITY, l_g = 0.f;
+            while (ok && co.next()) {
+                const uint32_t T = co.T;
+                if (co.first_tile()) { m_g = -INFINITY; l_g = 0.f; }
+                if ((T & 1u) == xb) {
+                    const uint32_t st = T % kStages;
+                    // this CTA's partial scores: out of TMEM, then to the peer
+                    float s[kTok];
+                    if (!(ok = wwait<false>(bar(B_SFULL + xb), (T >> 1) & 1, ctl))) break;
                     tc_fence_after();
-                }
-                if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
-                    for (int c = 0; c < kLatHalf / 16; ++c) {
-                        float o[16];
-                        tmem_ld16(tmem + lane_base + kColO + 16 * c, o);
-                        tmem_wait_ld();
-                        uint32_t u[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(o[j] * alpha);
-                        tmem_st16(tmem + lane_base + kColO + 16 * c, u);
+                    tmem_ld32(tmem + lane_base + kColS + 64 * xb, *reinterpret_cast<float(*)[32]>(&s[0]));
+                    tmem_ld32(tmem + lane_base + kColS + 64 * xb + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_SEMPTY + xb));
+                    // the peer has finished reading what this group sent for tile T - 2
+                    if (T >= 2 && !(ok = wwait<true>(bar(B_XEMPTY + xb), ((T >> 1) - 1) & 1, ctl))) break;
+                    if (i == 0) mbar_expect_tx(bar(B_XFULL + xb), kXBytes);      // the peer's copy of tile T
+                    {
+                        // block-scaled fp16: s = off + r with off the partial of the tile's first
+                        // row (always a row of the piece), so each r is rounded relative to the
+                        // spread of the partial within the tile, not to its magnitude
+                        // (|error| <= 2^-11 |s - off|); a difference beyond the fp16 range
+                        // saturates at +-65504 instead of becoming infinite
+                        const float off = s[0];
+    #pragma unroll
+                        for (int c = 0; c < kTok / 8; ++c) {
+                            uint32_t w[4];
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                w[e] = pack_half2_satfinite(s[8 * c + 2 * e] - off, s[8 * c + 2 * e + 1] - off);
+                            st_async_v4u(peer_x + (uint32_t)(c * kHeads + i) * 16, w[0], w[1], w[2], w[3], peer_xfull);
+                        }
+                        st_async_f32(peer_x + kXResBytes + (uint32_t)i * 4, off, peer_xfull);
                     }
-                }
-                {   // row i of P: 128 bytes, 16-byte chunk c stored at chunk c ^ (i & 7) (128B swizzle)
-                    uint8_t* prow = sm + kOffP + i * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *(uint4*)(prow + ((c ^ (i & 7)) << 4)) =
-                            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                }
-                if (valid < kTok) {
-                    // the value MMA must not see rows of the tile beyond the piece (they may
-                    // hold anything): zero them in this CTA's latent half of the stage
-                    uint8_t* stage = sm + kOffStage + st * kStageBytes;
-                    for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
-                        const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
-                        *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                    // add the peer's partial scores of tile T
+                    if (!(ok = wwait<true>(bar(B_XFULL + xb), (T >> 1) & 1, ctl))) break;
+                    {
+                        const uint8_t* xbase = sm + kOffX + xb * kXBytes;
+                        const uint4* xr = reinterpret_cast<const uint4*>(xbase) + i;
+                        const float off = reinterpret_cast<const float*>(xbase + kXResBytes)[i];
+    #pragma unroll
+                        for (int c = 0; c < kTok / 8; ++c) {
+                            const uint4 v = xr[c * kHeads];
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                                s[8 * c + 2 * e] += f.x + off;
+                                s[8 * c + 2 * e + 1] += f.y + off;
+                            }
+                        }
                     }
+                    mbar_arrive(bar(B_XCONS + xb));
+                    // rows past the end of this piece do not count (only the last tile of a
+                    // piece is partial)
+                    const int valid = co.valid_rows();
+                    if (valid < kTok) {
+    #pragma unroll
+                        for (int j = 0; j < kTok; ++j)
+                            if (j >= valid) s[j] = -INFINITY;
+                    }
+                    // tile maximum: eight running maxima, then a tree (short dependency chains)
+                    float m8[8];
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        m8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
+                                      fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
+    #pragma unroll
+                    for (int w = 4; w >= 1; w >>= 1)
+    #pragma unroll
+                        for (int j = 0; j < w; ++j) m8[j] = fmaxf(m8[j], m8[j + w]);
+                    const float mt = m8[0];
+                    // the running maximum after tile T - 1 (decided by the other group)
+                    if (T > 0) {
+                        if (!(ok = wwait<false>(bar(B_MH + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                        const float mp = mshare[((T - 1) & 1) * kHeads + i];
+                        if (!co.first_tile() && mp != m_g) { l_g *= fast_exp2(m_g - mp); m_g = mp; }
+                    }
+                    // lazy maximum: move it (and rescale) only when a score exceeds it by 2^8
+                    const bool need = mt > m_g + 8.f;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = fast_exp2(m_g - mt);
+                        m_g = mt;
+                        l_g *= alpha;
+                    }
+                    mshare[(T & 1) * kHeads + i] = m_g;
+                    mbar_arrive(bar(B_MH + (T & 1)));
+                    // P tile (bf16) for the value MMA; the sum uses the rounded values
+                    uint32_t packed[kTok / 2];
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums (short chains)
+    #pragma unroll
+                    for (int j = 0; j < kTok / 2; ++j) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(fast_exp2(s[2 * j] - m_g),
+                                                                        fast_exp2(s[2 * j + 1] - m_g));
+                        ls[j & 3] += __low2float(h2) + __high2float(h2);
+                        packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                    }
+                    l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    // the value MMA of the previous tile has finished with P and O
+                    if (T > 0) {
+                        if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                        tc_fence_after();
+                    }
+                    if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
+                        for (int c = 0; c < kLatHalf / 16; ++c) {
+                            float o[16];
+                            tmem_ld16(tmem + lane_base + kColO + 16 * c, o);
+                            tmem_wait_ld();
+                            uint32_t u[16];
+    #pragma unroll
+                            for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(o[j] * alpha);
+                            tmem_st16(tmem + lane_base + kColO + 16 * c, u);
+                        }
+                    }
+                    {   // row i of P: 128 bytes, 16-byte chunk c stored at chunk c ^ (i & 7) (128B swizzle)
+                        uint8_t* prow = sm + kOffP + i * 128;
+    #pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *(uint4*)(prow + ((c ^ (i & 7)) << 4)) =
+                                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                    }
+                    if (valid < kTok) {
+                        // the value MMA must not see rows of the tile beyond the piece (they may
+                        // hold anything): zero them in this CTA's latent half of the stage
+                        uint8_t* stage = sm + kOffStage + st * kStageBytes;
+                        for (int e = i; e < (kTok - valid) * 4 * 8; e += 128) {
+                            const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
+                            *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async_smem();                   // P (and zeroed rows) to the tensor core
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_PFULL));
                 }
-                fence_proxy_async_smem();                   // P (and zeroed rows) to the tensor core
+                if (co.last_tile()) {
+                    // this group's share of the piece's statistics
+                    float* sp = stats + ((co.si & 3) * 2 + grp) * 2 * kHeads;
+                    sp[i] = m_g;
+                    sp[kHeads + i] = l_g;
+                    mbar_arrive(bar(B_STATS + (co.si & 3)));
+                }
+            }
+        } else if (warp >= 12) {
+            // ------------------------------------------------------------ Q' loader / epilogue
+            reg_alloc_dec<96>();
+            const int i = tid - 384;                        // head row == TMEM lane
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            SegWalk walk;
+            walk.init(a.cum, a.wstart[g], g, S);
+            Seg cur, nxt;
+            bool have = walk.next(cur);
+            uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
+            // Q' of one piece into TMEM columns kColQ.. (zero rows for heads >= n_h)
+            auto load_q = [&](const Seg& sg) {
+                const bool row_ok = i < a.n_h;
+                const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
+                const uint4 zero = make_uint4(0, 0, 0, 0);
+                {   // rotary columns [512 + 32r, 512 + 32r + 32): the A operand of the rotary
+                    // score MMAs, in shared memory (row i: 64 bytes, 16-byte chunk c stored at
+                    // chunk c ^ ((i >> 1) & 3), the 64B swizzle)
+                    uint8_t* qrow = sm + kOffQR + i * 64;
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *(uint4*)(qrow + ((c ^ ((i >> 1) & 3)) << 4)) = row_ok ? src[64 + rank * 4 + c] : zero;
+                    fence_proxy_async_smem();
+                }
+                // latent columns [256r, 256r + 256) into tensor memory, two chunks of 64 bf16
+                // (32 TMEM columns each) per round of loads
+    #pragma unroll 1
+                for (int k = 0; k < 4; k += 2) {
+                    uint32_t r0[32], r1[32];
+    #pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = row_ok ? src[rank * 32 + 8 * k + c] : zero;
+                        const uint4 w = row_ok ? src[rank * 32 + 8 * k + 8 + c] : zero;
+                        r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
+                        r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
+                    }
+                    tmem_st32u(tmem + lane_base + kColQ + 32 * k, r0);
+                    tmem_st32u(tmem + lane_base + kColQ + 32 * k + 32, r1);
+                }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(B_PFULL));
-            }
-            if (co.last_tile()) {
-                // this group's share of the piece's statistics
-                float* sp = stats + ((co.si & 3) * 2 + grp) * 2 * kHeads;
-                sp[i] = m_g;
-                sp[kHeads + i] = l_g;
-                mbar_arrive(bar(B_STATS + (co.si & 3)));
-            }
-        }
-    } else if (warp >= 12) {
-        // ------------------------------------------------------------ Q' loader / epilogue
-        reg_alloc_dec<96>();
-        const int i = tid - 384;                        // head row == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        SegWalk walk;
-        walk.init(a.cum, a.wstart[g], g, S.per, S.total);
-        Seg cur, nxt;
-        bool have = walk.next(cur);
-        uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
-        // Q' of one piece into TMEM columns kColQ.. (zero rows for heads >= n_h)
-        auto load_q = [&](const Seg& sg) {
-            const bool row_ok = i < a.n_h;
-            const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-            {   // rotary columns [512 + 32r, 512 + 32r + 32): the A operand of the rotary
-                // score MMAs, in shared memory (row i: 64 bytes, 16-byte chunk c stored at
-                // chunk c ^ ((i >> 1) & 3), the 64B swizzle)
-                uint8_t* qrow = sm + kOffQR + i * 64;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *(uint4*)(qrow + ((c ^ ((i >> 1) & 3)) << 4)) = row_ok ? src[64 + rank * 4 + c] : zero;
-                fence_proxy_async_smem();
-            }
-            // latent columns [256r, 256r + 256) into tensor memory, two chunks of 64 bf16
-            // (32 TMEM columns each) per round of loads
-#pragma unroll 1
-            for (int k = 0; k < 4; k += 2) {
-                uint32_t r0[32], r1[32];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = row_ok ? src[rank * 32 + 8 * k + c] : zero;
-                    const uint4 w = row_ok ? src[rank * 32 + 8 * k + 8 + c] : zero;
-                    r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
-                    r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
+                mbar_arrive(bar(B_QFULL));
+            };
+            bool ok = true;
+            if (have) load_q(cur);
+            while (ok && have) {
+                t_end += (uint32_t)tiles_of(cur);
+                const bool more = walk.next(nxt);
+                if (more) {
+                    // the score MMAs of this piece are done with Q'
+                    if (!(ok = wwait<false>(bar(B_QEMPTY), si & 1, ctl))) break;
+                    tc_fence_after();
+                    load_q(nxt);
                 }
-                tmem_st32u(tmem + lane_base + kColQ + 32 * k, r0);
-                tmem_st32u(tmem + lane_base + kColQ + 32 * k + 32, r1);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(B_QFULL));
-        };
-        bool ok = true;
-        if (have) load_q(cur);
-        while (ok && have) {
-            t_end += (uint32_t)tiles_of(cur);
-            const bool more = walk.next(nxt);
-            if (more) {
-                // the score MMAs of this piece are done with Q'
-                if (!(ok = wwait<false>(bar(B_QEMPTY), si & 1, ctl))) break;
+                // epilogue of this piece: O_r / l, log2-sum-exp
+                if (!(ok = wwait<false>(bar(B_STATS + (si & 3)), (si >> 2) & 1, ctl))) break;
+                const float* sp = stats + (si & 3) * 4 * kHeads;
+                const float m0 = sp[i], l0 = sp[kHeads + i], m1 = sp[2 * kHeads + i], l1 = sp[3 * kHeads + i];
+                const float m_fin = fmaxf(m0, m1);
+                const float l_fin = l0 * exp2f(m0 - m_fin) + l1 * exp2f(m1 - m_fin);
+                if (!(ok = wwait<false>(bar(B_VDONE + ((t_end - 1) & 1)), ((t_end - 1) >> 1) & 1, ctl))) break;
                 tc_fence_after();
-                load_q(nxt);
-            }
-            // epilogue of this piece: O_r / l, log2-sum-exp
-            if (!(ok = wwait<false>(bar(B_STATS + (si & 3)), (si >> 2) & 1, ctl))) break;
-            const float* sp = stats + (si & 3) * 4 * kHeads;
-            const float m0 = sp[i], l0 = sp[kHeads + i], m1 = sp[2 * kHeads + i], l1 = sp[3 * kHeads + i];
-            const float m_fin = fmaxf(m0, m1);
-            const float l_fin = l0 * exp2f(m0 - m_fin) + l1 * exp2f(m1 - m_fin);
-            if (!(ok = wwait<false>(bar(B_VDONE + ((t_end - 1) & 1)), ((t_end - 1) >> 1) & 1, ctl))) break;
-            tc_fence_after();
-            const float inv = 1.f / l_fin;
-            const float lse2 = m_fin + log2f(l_fin);
-            const bool row_ok = i < a.n_h;
-            for (int c = 0; c < kLatHalf / 32; ++c) {
-                float o[32];
-                tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
-                tmem_wait_ld();
-                if (!row_ok) continue;
-                const int col = (int)rank * kLatHalf + 32 * c;
-                if (cur.complete) {
-                    __nv_bfloat16* dst = a.o_lat + ((int64_t)cur.b * a.n_h + i) * 512 + col;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * q + 2 * e] * inv, o[8 * q + 2 * e + 1] * inv);
-                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                const float inv = 1.f / l_fin;
+                const float lse2 = m_fin + log2f(l_fin);
+                const bool row_ok = i < a.n_h;
+                for (int c = 0; c < kLatHalf / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + kColO + 32 * c, o);
+                    tmem_wait_ld();
+                    if (!row_ok) continue;
+                    const int col = (int)rank * kLatHalf + 32 * c;
+                    if (cur.complete) {
+                        __nv_bfloat16* dst = a.o_lat + ((int64_t)cur.b * a.n_h + i) * 512 + col;
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t w[4];
+    #pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * q + 2 * e] * inv, o[8 * q + 2 * e + 1] * inv);
+                                w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                            }
+                            *(uint4*)(dst + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
                         }
-                        *(uint4*)(dst + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+                        float* dst = a.part_o + (cur.slot * a.n_h + i) * 512 + col;
+    #pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *(float4*)(dst + 4 * q) = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
+                                                                  o[4 * q + 2] * inv, o[4 * q + 3] * inv);
                     }
-                } else {
-                    float* dst = a.part_o + (cur.slot * a.n_h + i) * 512 + col;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *(float4*)(dst + 4 * q) = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv,
-                                                              o[4 * q + 2] * inv, o[4 * q + 3] * inv);
                 }
+                if (row_ok && rank == 0) {
+                    if (cur.complete) { if (a.lse) a.lse[(int64_t)cur.b * a.n_h + i] = lse2 * kLn2; }
+                    else a.part_l[cur.slot * a.n_h + i] = lse2;
+                }
+                tc_fence_before();
+                mbar_arrive(bar(B_OFREE));
+                cur = nxt;
+                have = more;
+                ++si;
             }
-            if (row_ok && rank == 0) {
-                if (cur.complete) { if (a.lse) a.lse[(int64_t)cur.b * a.n_h + i] = lse2 * kLn2; }
-                else a.part_l[cur.slot * a.n_h + i] = lse2;
-            }
-            tc_fence_before();
-            mbar_arrive(bar(B_OFREE));
-            cur = nxt;
-            have = more;
-            ++si;
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -737,7 +745,7 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
                             int64_t q_rows, const void* cache, int64_t cache_rows,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             const int32_t* wstart, void* o_lat, float* lse, float* part_o,
-                            float* part_l, int32_t* dev_status, cudaStream_t s) {
+                            float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl) {
     (void)q_rows;
     if (!get_encoder()) return cudaErrorNotSupported;
     CUtensorMap mc128, mc64;
@@ -745,15 +753,15 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
         !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     TcArgs a{(const __nv_bfloat16*)qp, row_off, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
-             lse, part_o, part_l, dev_status, d.n_heads, batch};
+             lse, part_o, part_l, dev_status, wait_limit_ns(), d.n_heads, batch};
     cudaError_t e = cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     profile_before_split(s);
-    split_tc_kernel<<<dim3(2 * workers), dim3(kThreads), kSmemBytes, s>>>(mc128, mc64, a);
+    e = launch_ex(split_tc_kernel, dim3(2 * workers), dim3(kThreads), kSmemBytes, s, pdl, mc128, mc64, a);
     profile_after_split(s);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

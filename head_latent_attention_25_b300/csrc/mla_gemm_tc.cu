@@ -28,7 +28,7 @@ constexpr int kGNMax = 128;           // tokens per tile (MMA N)
 constexpr int kGMaxStages = 8;        // ring depth is chosen per launch (stages <= this)
 constexpr int kGThreads = 128;
 constexpr uint32_t kATile = kGM * kGK * 2;      // 16 KB
-constexpr uint64_t kGTimeoutNs = 2000000000ull;
+constexpr uint64_t kGTimeoutNs = 2000000000ull;  // bound of the drain waits after an abort
 
 // Shared memory per token-tile width: the ring of stages x (A tile + B tile), reused by
 // the epilogue as a staging tile, then the barriers (offset chosen per launch).
@@ -47,6 +47,7 @@ struct GemmTcArgs {
     int chunks_per_split; // K chunks per CTA
     int k_splits;
     int a_mn;             // weights stored with the output feature contiguous (MN-major A)
+    int b_mn;             // B stored with the token index contiguous (MN-major B, NT >= 64)
     int m_split_tile;     // M tiles >= this read the second weight map (rows - tile offset)
     int a2_rows;          // rows loaded from the second weight map (<= 128)
     int mode;
@@ -55,17 +56,24 @@ struct GemmTcArgs {
     uint32_t off_bar;     // byte offset of the barriers: after the ring and the staging tile
     float alpha;
     void* y; int64_t y_g, y_tok;      // bf16 output: y[g*y_g + t*y_tok + m]
+    void* y2; int64_t y2_tok;         // bf16 output of the second map's rows (when set):
+                                      //   y2[t*y2_tok + m - m_split_tile*128]
     float* part; int part_ld;         // fp32 partial: part[(split*N + t)*part_ld + m]
     int32_t* dev_status;
+    uint64_t wait_ns;     // limit of every wait of the pipeline
 };
 
-__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* st) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* st,
+                                      uint64_t limit_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    // the hardware may suspend the thread inside try_wait for up to the hint: never
+    // longer than the limit itself
+    const uint32_t hint = limit_ns < 20000u ? (uint32_t)limit_ns : 20000u;
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kGTimeoutNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             if (st) atomicOr(st, MLA_DEV_TIMEOUT);
             return false;
@@ -127,13 +135,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    // the kernel behind this one in the same call may be scheduled now (it waits for this
+    // one's completion before it reads what this one writes)
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // producer
         uint32_t i = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++i) {
             const uint32_t st = i % NS;
-            if (!gwait(bar(E + st), ((i / NS) & 1) ^ 1, abort_flag, a.dev_status)) break;
+            if (!gwait(bar(E + st), ((i / NS) & 1) ^ 1, abort_flag, a.dev_status, a.wait_ns)) break;
             const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
             mbar_expect_tx(bar(st), a_bytes + kBTile);
             if (second) {
@@ -144,7 +156,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             } else {
                 tma_load_3d(sa, &map_a, kc * kGK, m_tile * kGM, g, bar(st));
             }
-            tma_load_3d(sb, &map_b, kc * kGK, g, n_tile * NT, bar(st));
+            if (a.b_mn) {
+                // 64-token halves of the tile, 64 K rows each (one 128-byte swizzle atom wide)
+                for (int j = 0; j < NT / 64; ++j)
+                    tma_load_3d(sb + j * (kGK * 128), &map_b, n_tile * NT + 64 * j, kc * kGK, g, bar(st));
+            } else {
+                tma_load_3d(sb, &map_b, kc * kGK, g, n_tile * NT, bar(st));
+            }
         }
         for (uint32_t k = 0; k < NS && k < i; ++k) {
             const uint32_t j = i - 1 - k;
@@ -152,19 +170,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer
-        const uint32_t idesc = idesc_bf16_f32(kGM, NT, a.a_mn && !second ? 1u : 0u, 0u);
+        const uint32_t idesc = idesc_bf16_f32(kGM, NT, a.a_mn && !second ? 1u : 0u, a.b_mn ? 1u : 0u);
         uint32_t i = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++i) {
             const uint32_t st = i % NS;
-            if (!gwait(bar(st), (i / NS) & 1, abort_flag, a.dev_status)) break;
+            if (!gwait(bar(st), (i / NS) & 1, abort_flag, a.dev_status, a.wait_ns)) break;
             tc_fence_after();
             const uint32_t sa = base + st * L::kStage, sb = sa + kATile;
             for (int k = 0; k < kGK / 16; ++k) {
                 const uint64_t da = (a.a_mn && !second)
                     ? smem_desc(sa + 2048 * k, kATile / 2, 1024, kSwizzle128B)   // MN-major: 64-wide atoms 8 KB apart
                     : smem_desc(sa + 32 * k, 16, 1024, kSwizzle128B);
-                mma_bf16(tmem, da, smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B), idesc,
-                         (i > 0 || k > 0) ? 1u : 0u);
+                const uint64_t db = a.b_mn
+                    ? smem_desc(sb + 2048 * k, kGK * 128, 1024, kSwizzle128B)    // MN-major: 64-token atoms 8 KB apart
+                    : smem_desc(sb + 32 * k, 16, 1024, kSwizzle128B);
+                mma_bf16(tmem, da, db, idesc, (i > 0 || k > 0) ? 1u : 0u);
             }
             mma_commit(bar(E + st));
         }
@@ -172,7 +192,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     // epilogue: thread <-> output feature (TMEM lane), 32 tokens per TMEM load
     __syncwarp();
-    const bool ok = gwait(bar(DONE), 0, abort_flag, a.dev_status);
+    const bool ok = gwait(bar(DONE), 0, abort_flag, a.dev_status, a.wait_ns);
     tc_fence_after();
     const int m = m_tile * kGM + warp * 32 + lane;
     const bool m_ok = m < a.M;
@@ -198,7 +218,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
             for (int j = 0; j < kCols; ++j) {
                 const int t = n_tile * NT + 32 * c + j;
                 if (t >= a.N) break;
-                if (a.mode == kOutBf16)
+                if (a.mode == kOutBf16 && second && a.y2)
+                    ((__nv_bfloat16*)a.y2)[(int64_t)t * a.y2_tok + m - a.m_split_tile * kGM] =
+                        __float2bfloat16_rn(a.alpha * v[j]);
+                else if (a.mode == kOutBf16)
                     ((__nv_bfloat16*)a.y)[(int64_t)g * a.y_g + (int64_t)t * a.y_tok + m] =
                         __float2bfloat16_rn(a.alpha * v[j]);
                 else
@@ -220,11 +243,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
                     w[q] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                *reinterpret_cast<uint4*>((__nv_bfloat16*)a.y + (int64_t)g * a.y_g + (int64_t)t * a.y_tok +
-                                          m_tile * kGM + 8 * f8) = make_uint4(w[0], w[1], w[2], w[3]);
+                __nv_bfloat16* dst = (second && a.y2)
+                    ? (__nv_bfloat16*)a.y2 + (int64_t)t * a.y2_tok + (m_tile - a.m_split_tile) * kGM + 8 * f8
+                    : (__nv_bfloat16*)a.y + (int64_t)g * a.y_g + (int64_t)t * a.y_tok + m_tile * kGM + 8 * f8;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
     }
+    // after an abort the epilogue did not wait for the MMAs: every MMA (the issuer's
+    // DONE commit follows its last one in both paths) completes before TMEM is freed
+    if (!all_ok && warp == 2) gdrain(bar(DONE), 0);
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
@@ -248,6 +276,7 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
                        const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
                        int64_t cache_rows, __nv_bfloat16* __restrict__ cache, int32_t* dev_status) {
     __shared__ float2 red[kFinGroups][kFinPairs];
+    pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
     const int t = blockIdx.x;
     const int width = d_c + d_r;
     const int x = threadIdx.x % kFinPairs, y = threadIdx.x / kFinPairs;
@@ -289,6 +318,36 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
         v1 = r1;
     }
     *(__nv_bfloat162*)(cache + (off + pos) * width + e) = __floats2bfloat162_rn(v0, v1);
+}
+
+// y[t, e] = bf16(sum over splits of part[split, t, e]) for a split-K GEMM, summed in a
+// fixed order (8 thread groups per column pair, then a shared-memory reduction), so the
+// result does not depend on timing.  Grid (token, column-pair groups of kFinPairs).
+__global__ void __launch_bounds__(kFinPairs * kFinGroups)
+splitk_reduce_kernel(const float* __restrict__ part, int k_splits, int n_tok, int width,
+                     __nv_bfloat16* __restrict__ y, int64_t y_tok) {
+    __shared__ float2 red[kFinGroups][kFinPairs];
+    pdl_wait();                 // launched behind the split-K GEMM: its partial sums are complete
+    const int t = blockIdx.x;
+    const int x = threadIdx.x % kFinPairs, g = threadIdx.x / kFinPairs;
+    const int e = 2 * (blockIdx.y * kFinPairs + x);
+    float2 acc = make_float2(0.f, 0.f);
+    if (e < width) {
+        const float* p = part + (int64_t)t * width + e;
+        const int64_t split_stride = (int64_t)n_tok * width;
+        for (int s0 = g; s0 < k_splits; s0 += kFinGroups) {
+            const float2 v = *reinterpret_cast<const float2*>(p + s0 * split_stride);
+            acc.x += v.x;
+            acc.y += v.y;
+        }
+    }
+    red[g][x] = acc;
+    __syncthreads();
+    if (g != 0 || e >= width) return;
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < kFinGroups; ++q) { v0 += red[q][x].x; v1 += red[q][x].y; }
+    *(__nv_bfloat162*)(y + (int64_t)t * y_tok + e) = __floats2bfloat162_rn(v0, v1);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -336,7 +395,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtens
     while (stages > 1 && (uint32_t)stages * stage_bytes + 256 + 1024 > 232448u) --stages;
     a.stages = max(stages, 1);
     a.staged = a.mode == kOutBf16 && a.M % kGM == 0 && (a.y_tok % 8) == 0 && (a.y_g % 8) == 0 &&
-               ((uintptr_t)a.y % 16) == 0;
+               ((uintptr_t)a.y % 16) == 0 && (!a.y2 || ((a.y2_tok % 8) == 0 && ((uintptr_t)a.y2 % 16) == 0));
     const uint32_t tile_bytes = (uint32_t)nt * (kGM + 4) * 4;
     uint32_t ring = (uint32_t)a.stages * stage_bytes;
     if (a.staged && tile_bytes > ring) ring = (tile_bytes + 1023) / 1024 * 1024;
@@ -370,6 +429,7 @@ GemmTcArgs gblank() {
     a.m_split_tile = 1 << 30;
     a.alpha = 1.f;
     a.mode = kOutBf16;
+    a.wait_ns = wait_limit_ns();
     return a;
 }
 
@@ -380,17 +440,167 @@ bool gemm_tc_shapes_ok(const mla_dims& d) {
            d.hidden % 64 == 0;
 }
 
-size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count) {
-    const int k_chunks = (d.hidden + kGK - 1) / kGK;
-    const int m_tiles = (d.d_c + d.d_r + kGM - 1) / kGM;
+// Splits of a long reduction (K) across CTAs so that the M x N tiles times the splits
+// fill the GPU about once; at least two 64-wide chunks per split.
+int k_splits_for(int K, int M, int n_tok, int sm_count) {
+    const int k_chunks = (K + kGK - 1) / kGK;
+    const int m_tiles = (M + kGM - 1) / kGM;
     const int n_tiles = (n_tok + kGNMax - 1) / kGNMax;
     int want = (sm_count > 0 ? sm_count : 148) / (m_tiles * n_tiles);
     if (want < 1) want = 1;
     int per = (k_chunks + want - 1) / want;
     if (per < 2) per = 2;
-    const int splits = (k_chunks + per - 1) / per;
+    return (k_chunks + per - 1) / per;
+}
+
+size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count) {
+    const int splits = k_splits_for(d.hidden, d.d_c + d.d_r, n_tok, sm_count);
     if (k_splits_out) *k_splits_out = splits;
     return align_up((size_t)splits * n_tok * (d.d_c + d.d_r) * sizeof(float), 256);
+}
+
+size_t query_latent_tc_workspace(int hidden, int d_q, int n_tok, int* k_splits_out, int sm_count) {
+    const int splits = k_splits_for(hidden, d_q, n_tok, sm_count);
+    if (k_splits_out) *k_splits_out = splits;
+    return align_up((size_t)splits * n_tok * d_q * sizeof(float), 256);
+}
+
+cudaError_t launch_query_latent_tc(int hidden, int d_q, int batch, const void* h, const void* w_dq,
+                                   void* workspace, void* c_q, int32_t* dev_status, int sm_count,
+                                   cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    int splits = 1;
+    query_latent_tc_workspace(hidden, d_q, batch, &splits, sm_count);
+    const int nt = pick_nt(batch);
+    const uint64_t H = hidden;
+    CUtensorMap ma, mb;
+    // W_DQ [d_q, hidden] (K-major), h [batch, hidden]
+    if (!map3(&ma, w_dq, H, d_q, 1, H * 2, H * 2 * d_q, kGK, kGM, 1) ||
+        !map3(&mb, h, H, 1, batch, H * 2, H * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = d_q;
+    a.N = batch;
+    a.k_chunks = (hidden + kGK - 1) / kGK;
+    a.k_splits = splits;
+    a.chunks_per_split = (a.k_chunks + splits - 1) / splits;
+    a.mode = kOutPartial;
+    a.part = (float*)workspace;
+    a.part_ld = d_q;
+    a.dev_status = dev_status;
+    cudaError_t e = run_gemm(ma, ma, mb, a, 1, nt, s);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(batch, (d_q / 2 + kFinPairs - 1) / kFinPairs);
+    e = launch_ex(splitk_reduce_kernel, grid, dim3(kFinPairs * kFinGroups), 0, s, true, (const float*)workspace,
+                  splits, batch, d_q, (__nv_bfloat16*)c_q, (int64_t)d_q);
+    note_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Split-K product u[t, m] = sum_k A[m, k] x[t, k] for a long K, then the fixed-order
+// reduction of the partial sums to bf16 u[t*u_tok + m].  ma: the A map (K-major, or
+// MN-major when a_mn), mb: x as [batch, K].
+cudaError_t splitk_linear(const CUtensorMap& ma, const CUtensorMap& mb, int a_mn, int M, int K, int batch,
+                          void* workspace, void* u, int64_t u_tok, int32_t* dev_status, int sm_count,
+                          cudaStream_t s) {
+    const int splits = k_splits_for(K, M, batch, sm_count);
+    GemmTcArgs a = gblank();
+    a.M = M;
+    a.N = batch;
+    a.k_chunks = (K + kGK - 1) / kGK;
+    a.k_splits = splits;
+    a.chunks_per_split = (a.k_chunks + splits - 1) / splits;
+    a.a_mn = a_mn;
+    a.mode = kOutPartial;
+    a.part = (float*)workspace;
+    a.part_ld = M;
+    a.dev_status = dev_status;
+    cudaError_t e = run_gemm(ma, ma, mb, a, 1, pick_nt(batch), s);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(batch, (M / 2 + kFinPairs - 1) / kFinPairs);
+    e = launch_ex(splitk_reduce_kernel, grid, dim3(kFinPairs * kFinGroups), 0, s, true, (const float*)workspace,
+                  splits, batch, M, (__nv_bfloat16*)u, u_tok);
+    note_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+size_t output_tc_workspace(int hidden, int k_in, int n_tok, int sm_count) {
+    return align_up((size_t)k_splits_for(k_in, hidden, n_tok, sm_count) * n_tok * hidden * sizeof(float), 256);
+}
+
+cudaError_t launch_output_tc(const mla_dims& d, int batch, const void* o, const void* w_o, void* workspace,
+                             void* u, int32_t* dev_status, int sm_count, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const uint64_t K = (uint64_t)d.n_heads * d.d_h, H = d.hidden;
+    CUtensorMap ma, mb;
+    // W_O [hidden, n_h*d_h] (K-major), o [batch, n_h*d_h]
+    if (!map3(&ma, w_o, K, H, 1, K * 2, K * 2 * H, kGK, kGM, 1) ||
+        !map3(&mb, o, K, 1, batch, K * 2, K * 2, kGK, 1, pick_nt(batch)))
+        return cudaErrorInvalidValue;
+    return splitk_linear(ma, mb, 0, d.hidden, (int)K, batch, workspace, u, d.hidden, dev_status, sm_count, s);
+}
+
+cudaError_t launch_output_merged_tc(const mla_dims& d, int batch, const void* o_lat, const void* w_ov,
+                                    void* workspace, void* u, int32_t* dev_status, int sm_count, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const uint64_t K = (uint64_t)d.n_heads * d.d_c, H = d.hidden;
+    CUtensorMap ma, mb;
+    // W_OV stored [n_h * d_c, hidden]: the output feature contiguous (MN-major A), o_lat [batch, n_h*d_c]
+    if (!map3(&ma, w_ov, H, K, 1, H * 2, H * 2 * K, 64, kGK, 1) ||
+        !map3(&mb, o_lat, K, 1, batch, K * 2, K * 2, kGK, 1, pick_nt(batch)))
+        return cudaErrorInvalidValue;
+    return splitk_linear(ma, mb, 1, d.hidden, (int)K, batch, workspace, u, d.hidden, dev_status, sm_count, s);
+}
+
+cudaError_t launch_merge_output_weights_tc(const mla_dims& d, const void* w_o, const void* w_uv, void* w_ov,
+                                           int32_t* dev_status, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const uint64_t H = d.hidden, nh = d.n_heads, dh = d.d_h, dc = d.d_c;
+    CUtensorMap ma, mb;
+    // A = W_O^(i): rows m of W_O, columns i*d_h .. i*d_h + d_h - 1 (K-major, head = 3rd dim);
+    // B = W_UV^(i) read as [d_c tokens x d_h] with the token index contiguous (MN-major)
+    if (!map3(&ma, w_o, dh, H, nh, nh * dh * 2, dh * 2, kGK, kGM, 1) ||
+        !map3(&mb, w_uv, dc, dh, nh, dc * 2, dh * dc * 2, 64, kGK, 1))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = d.hidden;
+    a.N = d.d_c;
+    a.k_chunks = (d.d_h + kGK - 1) / kGK;
+    a.chunks_per_split = a.k_chunks;
+    a.b_mn = 1;
+    a.y = w_ov;                        // W_OV^(i)[c][m] at i*d_c*hidden + c*hidden + m
+    a.y_g = (int64_t)d.d_c * d.hidden;
+    a.y_tok = d.hidden;
+    a.dev_status = dev_status;
+    return run_gemm(ma, ma, mb, a, d.n_heads, kGNMax, s);
+}
+
+cudaError_t launch_project_query_tc(const mla_dims& d, int batch, int d_in, const void* x, const void* w_uq,
+                                    const void* w_qr, void* q_c, void* q_r, int32_t* dev_status,
+                                    cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const int nt = pick_nt(batch);
+    const uint64_t K = d_in;
+    const int m1 = d.n_heads * d.d_h, m2 = d.n_heads * d.d_r;
+    CUtensorMap ma, ma2, mb;
+    // [W_UQ ; W_QR] as one M range: tiles below m1/128 read W_UQ, the rest W_QR
+    if (!map3(&ma, w_uq, K, m1, 1, K * 2, K * 2 * m1, kGK, kGM, 1) ||
+        !map3(&ma2, w_qr, K, m2, 1, K * 2, K * 2 * m2, kGK, kGM, 1) ||
+        !map3(&mb, x, K, 1, batch, K * 2, K * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = m1 + m2;
+    a.N = batch;
+    a.k_chunks = (d_in + kGK - 1) / kGK;
+    a.chunks_per_split = a.k_chunks;
+    a.m_split_tile = m1 / kGM;
+    a.a2_rows = kGM;
+    a.y = q_c;
+    a.y_tok = m1;
+    a.y2 = q_r;
+    a.y2_tok = m2;
+    a.dev_status = dev_status;
+    return run_gemm(ma, ma2, mb, a, 1, nt, s);
 }
 
 cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
@@ -425,12 +635,11 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
     cudaError_t e = run_gemm(ma, ma2, mb, a, 1, nt, s);
     if (e != cudaSuccess) return e;
     const dim3 fin_grid(n_tok, (width / 2 + kFinPairs - 1) / kFinPairs);
-    append_finalize_kernel<<<fin_grid, kFinPairs * kFinGroups, 0, s>>>((const float*)workspace, splits, n_tok, n_new,
-                                                          d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
-                                                          row_off, cap, pos0, cache_rows,
-                                                          (__nv_bfloat16*)cache, dev_status);
+    e = launch_ex(append_finalize_kernel, fin_grid, dim3(kFinPairs * kFinGroups), 0, s, true,
+                  (const float*)workspace, splits, n_tok, n_new, d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
+                  row_off, cap, pos0, cache_rows, (__nv_bfloat16*)cache, dev_status);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const void* w_uk, float alpha,

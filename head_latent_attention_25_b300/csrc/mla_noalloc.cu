@@ -8,9 +8,9 @@
 // until the process exits.
 //
 // In host code `g_decode_scratch` names a host-side stand-in, not device memory, so
-// it is never passed to a kernel directly: the device address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) and cached.
-#include <mutex>
+// it is never passed to a kernel directly: every call looks the device address up with
+// cudaGetSymbolAddress on the current device (no cached address can outlive a reset of
+// the device's context).
 
 #include "mla_common.cuh"
 #include "mla_internal.h"
@@ -18,25 +18,14 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;     // 32 MiB per device
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on first use).
+// Device address of the scratch array on the current device.
 mla_status scratch_of_current_device(void** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+    *out = p;
     return MLA_OK;
 }
 

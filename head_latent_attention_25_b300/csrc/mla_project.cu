@@ -148,11 +148,18 @@ __global__ void __launch_bounds__(256) fold_rope_kernel(const Tin* __restrict__ 
                                                         int d_r, double rope_r, float alpha,
                                                         ScheduleArgs sch) {
     __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
+    // Launched right behind the fold GEMM (programmatic dependent launch), this kernel
+    // touches nothing that GEMM reads or writes (the GEMM fills Q' columns [0, d_c), this
+    // kernel columns [d_c, d_c + d_r) and the schedule), so it runs beside it and only
+    // waits for it at the end: its own completion then implies the GEMM's, which is what
+    // the attention kernel behind it waits for.
+    pdl_trigger();
     const int b = blockIdx.x;
     if (b == gridDim.x - 1 && sch.cum) {
         // one extra column of blocks: its first block builds the split schedule, which
         // saves the decode a launch (it depends only on seq_len and row_off)
         if (blockIdx.y == 0) build_schedule(sch);
+        pdl_wait();
         return;
     }
     const int h0 = blockIdx.y * kRopeHeads;
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(256) fold_rope_kernel(const Tin* __restrict__ 
         st2(qp + ((int64_t)b * n_h + i) * (d_c + d_r) + d_c + 2 * k,
             alpha * (x.x * cs[k] - x.y * sn[k]), alpha * (x.x * sn[k] + x.y * cs[k]));
     }
+    pdl_wait();
 }
 
 }  // namespace
@@ -204,6 +212,16 @@ cudaError_t launch_project_query(const mla_dims& d, bool bf16, int batch, int d_
     return dispatch(a, bf16, bf16, s);
 }
 
+cudaError_t launch_query_latent(const mla_dims& d, bool bf16, int batch, int d_q, const void* h,
+                                const void* w_dq, void* c_q, cudaStream_t s) {
+    GemmArgs a = blank();
+    a.x = h; a.x_m = d.hidden;
+    a.w = w_dq; a.w_n = d.hidden; a.w_k = 1;
+    a.y = c_q; a.y_m = d_q;
+    a.G = 1; a.M = batch; a.N = d_q; a.K = d.hidden;
+    return dispatch(a, bf16, bf16, s);
+}
+
 cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_c,
                         const void* q_r, const void* w_uk, const int32_t* seq_len, float alpha,
                         void* qp, cudaStream_t s) {
@@ -216,30 +234,32 @@ cudaError_t launch_fold(const mla_dims& d, bool in_bf16, bool out_bf16, int batc
     a.alpha = alpha;
     cudaError_t e = dispatch(a, in_bf16, out_bf16, s);
     if (e != cudaSuccess) return e;
-    return launch_fold_rope(d, in_bf16, out_bf16, batch, q_r, seq_len, alpha, qp, s, nullptr);
+    return launch_fold_rope(d, in_bf16, out_bf16, batch, q_r, seq_len, alpha, qp, s, nullptr, false);
 }
 
 cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
                              const int32_t* seq_len, float alpha, void* qp, cudaStream_t s,
-                             const ScheduleArgs* sched_args) {
+                             const ScheduleArgs* sched_args, bool pdl) {
     if (d.d_r / 2 > kMaxRopePairs) return cudaErrorInvalidValue;
     ScheduleArgs sch{};
     if (sched_args) sch = *sched_args;
     const dim3 grid(batch + (sched_args ? 1 : 0), (d.n_heads + kRopeHeads - 1) / kRopeHeads);
     const double r = rope_ratio(d.rope_base, d.d_r);
+    cudaError_t e;
     if (in_bf16) {
         if (out_bf16)
-            fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
+            e = launch_ex(fold_rope_kernel<__nv_bfloat16, __nv_bfloat16>, grid, dim3(256), 0, s, pdl,
+                          (const __nv_bfloat16*)q_r, seq_len, (__nv_bfloat16*)qp, d.n_heads, d.d_c, d.d_r, r,
+                          alpha, sch);
         else
-            fold_rope_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)q_r, seq_len,
-                (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
+            e = launch_ex(fold_rope_kernel<__nv_bfloat16, float>, grid, dim3(256), 0, s, pdl,
+                          (const __nv_bfloat16*)q_r, seq_len, (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
     } else {
-        fold_rope_kernel<<<grid, 256, 0, s>>>((const float*)q_r, seq_len, (float*)qp,
-            d.n_heads, d.d_c, d.d_r, r, alpha, sch);
+        e = launch_ex(fold_rope_kernel<float, float>, grid, dim3(256), 0, s, pdl, (const float*)q_r, seq_len,
+                      (float*)qp, d.n_heads, d.d_c, d.d_r, r, alpha, sch);
     }
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const void* o_lat,

@@ -24,8 +24,9 @@ struct ScheduleArgs {
 __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
     __shared__ long long warp_tot[32];
     __shared__ long long carry;
+    __shared__ unsigned long long longest;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
-    if (tid == 0) carry = 0;
+    if (tid == 0) { carry = 0; longest = 0; }
     __syncthreads();
     for (int base = 0; base < a.batch; base += nt) {
         const int i = base + tid;
@@ -34,6 +35,7 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
             const long long n = a.seq_len[i], o = a.row_off[i];
             if (n >= 1 && o >= 0 && o + n <= a.cache_rows) x = n;
             else atomicOr(a.dev_status, MLA_DEV_BAD_LENGTH);
+            atomicMax(&longest, (unsigned long long)x);
         }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -60,6 +62,11 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
     }
     const long long total = carry;
     const int64_t per = total > 0 ? (total + a.workers - 1) / a.workers : 1;
+    // Whole sequences per worker when there are no more sequences than workers and the
+    // longest is within a quarter of the equal share: a little more time on the busiest
+    // worker buys no cut sequence (no partial results, no merge, no mid-range reload of
+    // the folded query).
+    const bool whole = a.batch <= a.workers && (long long)longest <= per + per / 4;
     if (tid == 0) {
         a.cum[0] = 0;
         Schedule s;
@@ -67,12 +74,17 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
         s.workers = a.workers;
         s.batch = a.batch;
         s.per = per;
+        s.whole = whole ? 1 : 0;
         *a.sched = s;
     }
     __syncthreads();                            // cum complete and visible to the block
     // first sequence of each worker's range: the last sequence whose rows start at or
     // before the range start (saves every role of the split kernels a binary search)
     for (int g = tid; g < a.workers; g += nt) {
+        if (whole) {
+            a.wstart[g] = g < a.batch ? g : a.batch - 1;
+            continue;
+        }
         const int64_t cur = (int64_t)g * per;
         int lo = 0, hi = a.batch - 1;
         while (lo < hi) {

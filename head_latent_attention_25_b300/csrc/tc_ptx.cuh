@@ -143,6 +143,14 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float a, uint
                  ::"r"(remote_addr), "r"(__float_as_uint(a)), "r"(remote_bar) : "memory");
 }
 
+// Two fp32 values rounded to fp16 (nearest even) and packed, `lo` in the low half;
+// values beyond the fp16 range become +-65504 instead of +-inf.
+__device__ __forceinline__ uint32_t pack_half2_satfinite(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
                                             int32_t y, uint32_t bar) {

@@ -24,17 +24,25 @@ class DecodeStep:
 
     def __init__(self, *, n_heads: int, d_h: int, d_c: int, d_r: int, hidden: int,
                  dtype: str, ctx_lens: Sequence[int], n_new: int, rope_base: float = 10000.0,
-                 softmax_scale: float = 0.0, query_from_h: bool = False, d_q_in: Optional[int] = None,
-                 num_splits: int = 0, extra_rows: int = 0, device: str = "cuda"):
+                 softmax_scale: float = 0.0, query_from_h: bool = False, d_q: Optional[int] = None,
+                 n_q: int = 1, num_splits: int = 0, extra_rows: int = 0, device: str = "cuda"):
         L.load()
         self.dims = L.make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base, softmax_scale)
         self.dt = L.MLA_BF16 if dtype == "bf16" else L.MLA_F32
         self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
         self.batch = B = len(ctx_lens)
         self.n_new = n_new
+        # n_q > 1: that many causal queries per sequence (the last n_q positions)
+        self.n_q = n_q
+        if n_q > 1 and query_from_h:
+            raise ValueError("several queries per sequence come with given q_C, q_R")
+        Q = (n_q,) if n_q > 1 else ()
         self.ctx_lens = [int(x) for x in ctx_lens]
         self.query_from_h = query_from_h
-        self.d_q_in = d_q_in if d_q_in is not None else hidden
+        # with a query latent (d_q), c_q = W_DQ h first; without one the query parts come
+        # from h itself
+        self.d_q = d_q if query_from_h else None
+        self.d_q_in = self.d_q if self.d_q else hidden
         self.row_elems = d_c + d_r
         self.device = device
         caps = [c + n_new + extra_rows for c in self.ctx_lens]
@@ -53,20 +61,27 @@ class DecodeStep:
         # on a 256-byte boundary), so a caller can move them with one copy
         def _round(n):
             return (n + 127) // 128 * 128
-        n_h, n_c, n_r = B * n_new * hidden, B * n_heads * d_h, B * n_heads * d_r
+        n_h, n_c, n_r = B * n_new * hidden, B * n_q * n_heads * d_h, B * n_q * n_heads * d_r
         o_c = _round(n_h)
         o_r = o_c + _round(n_c)
         self.inputs = torch.zeros(o_r + _round(n_r), dtype=self.tdt, device=device)
         self.h = self.inputs[:n_h].view(B, n_new, hidden)
-        self.q_c = self.inputs[o_c:o_c + n_c].view(B, n_heads, d_h)
-        self.q_r = self.inputs[o_r:o_r + n_r].view(B, n_heads, d_r)
-        self.x_q = torch.zeros(B, self.d_q_in, dtype=self.tdt, device=device) if query_from_h else None
-        self.o_lat = torch.zeros(B, n_heads, d_c, dtype=self.tdt, device=device)
-        self.lse = torch.zeros(B, n_heads, dtype=torch.float32, device=device)
-        self.out = torch.zeros(B, n_heads, d_h, dtype=self.tdt, device=device)
+        self.q_c = self.inputs[o_c:o_c + n_c].view(B, *Q, n_heads, d_h)
+        self.q_r = self.inputs[o_r:o_r + n_r].view(B, *Q, n_heads, d_r)
+        self.x_q = torch.zeros(B, hidden, dtype=self.tdt, device=device) if query_from_h else None
+        self.c_q = torch.zeros(B, self.d_q, dtype=self.tdt, device=device) if self.d_q else None
+        self.q_ws_bytes = (L.mla_query_latent_workspace_size(self.dims, self.dt, B, self.d_q)
+                           if self.d_q else 0)
+        self.q_workspace = torch.empty(max(self.q_ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.o_lat = torch.zeros(B, *Q, n_heads, d_c, dtype=self.tdt, device=device)
+        self.lse = torch.zeros(B, *Q, n_heads, dtype=torch.float32, device=device)
+        self.out = torch.zeros(B, *Q, n_heads, d_h, dtype=self.tdt, device=device)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
         self.num_splits = num_splits
-        self.ws_bytes = L.mla_decode_workspace_size(self.dims, self.dt, B, self.max_seq_len, num_splits)
+        self.ws_bytes = (L.mla_decode_workspace_size(self.dims, self.dt, B, self.max_seq_len, num_splits)
+                         if n_q == 1 else
+                         L.mla_decode_multi_workspace_size(self.dims, self.dt, B, n_q, self.max_seq_len,
+                                                           num_splits))
         if self.ws_bytes == 0:
             raise L.MlaError("mla_decode_workspace_size", L.MLA_ERR_UNSUPPORTED)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
@@ -79,6 +94,14 @@ class DecodeStep:
     def set_weights(self, weights: dict):
         for k, v in weights.items():
             self.w[k] = v.to(self.device, self.tdt).contiguous()
+        if "w_o" in self.w:
+            # the layer output after the step: u = W_O [o_1; ...; o_n_h], two-step or merged
+            B = self.batch * self.n_q
+            self.u = torch.zeros(B, self.dims.hidden, dtype=self.tdt, device=self.device)
+            self.out_ws_bytes = max(L.mla_output_workspace_size(self.dims, self.dt, B, False),
+                                    L.mla_output_workspace_size(self.dims, self.dt, B, True))
+            self.out_workspace = torch.empty(max(self.out_ws_bytes, 256), dtype=torch.uint8, device=self.device)
+            self.w_ov = None
 
     def set_prefill(self, b: int, rows: torch.Tensor):
         n = rows.shape[0]
@@ -102,12 +125,26 @@ class DecodeStep:
                            stream)
 
     def project_query(self, stream=None):
-        L.mla_project_query(self.dims, self.dt, self.batch, self.d_q_in, self.x_q, self.w["w_uq"],
-                            self.w["w_qr"], self.q_c, self.q_r, stream)
+        if self.d_q:
+            L.mla_project_query_latent(self.dims, self.dt, self.batch, self.d_q, self.x_q, self.w["w_dq"],
+                                       self.q_workspace, self.q_ws_bytes, self.c_q, self.dev_status, stream)
+        L.mla_project_query(self.dims, self.dt, self.batch, self.d_q_in, self.c_q if self.d_q else self.x_q,
+                            self.w["w_uq"], self.w["w_qr"], self.q_c, self.q_r, self.dev_status, stream)
 
     def decode(self, stream=None, num_splits=None, o_lat=None, lse=None):
         ns = self.num_splits if num_splits is None else num_splits
         ws = self.workspace
+        if self.n_q > 1:
+            if ns != self.num_splits:
+                nb = L.mla_decode_multi_workspace_size(self.dims, self.dt, self.batch, self.n_q,
+                                                       self.max_seq_len, ns)
+                ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
+            L.mla_decode_absorbed_multi(self.dims, self.dt, self.batch, self.n_q, self.q_c, self.q_r,
+                                        self.w["w_uk"], self.cache, self.total_rows, self.row_off,
+                                        self.seq_len, self.max_seq_len, ns, ws, ws.numel(),
+                                        self.o_lat if o_lat is None else o_lat,
+                                        self.lse if lse is None else lse, self.dev_status, stream)
+            return
         if ns != self.num_splits:
             nb = L.mla_decode_workspace_size(self.dims, self.dt, self.batch, self.max_seq_len, ns)
             ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
@@ -131,8 +168,25 @@ class DecodeStep:
         L.mla_decode_attend(*self._decode_args(), stream)
 
     def project_out(self, stream=None):
-        L.mla_project_out(self.dims, self.dt, self.batch, self.o_lat, self.w["w_uv"], self.out,
+        L.mla_project_out(self.dims, self.dt, self.batch * self.n_q, self.o_lat, self.w["w_uv"], self.out,
                           self.dev_status, stream)
+
+    def project_output(self, stream=None):
+        """u = W_O [o_1; ...; o_n_h] from the step's per-head outputs."""
+        L.mla_project_output(self.dims, self.dt, self.batch * self.n_q, self.out, self.w["w_o"],
+                             self.out_workspace, self.out_ws_bytes, self.u, self.dev_status, stream)
+
+    def merge_output_weights(self, stream=None):
+        """W_OV^(i) = W_O^(i) W_UV^(i) ([n_h, d_c, hidden]), once."""
+        d = self.dims
+        self.w_ov = torch.empty(d.n_heads, d.d_c, d.hidden, dtype=self.tdt, device=self.device)
+        L.mla_merge_output_weights(d, self.dt, self.w["w_o"], self.w["w_uv"], self.w_ov, self.dev_status, stream)
+
+    def project_output_merged(self, u=None, stream=None):
+        """u = sum_i W_OV^(i) o_lat_i straight from the latent output."""
+        L.mla_project_output_merged(self.dims, self.dt, self.batch * self.n_q, self.o_lat, self.w_ov,
+                                    self.out_workspace, self.out_ws_bytes, self.u if u is None else u,
+                                    self.dev_status, stream)
 
     def step(self, stream=None):
         """The whole path: append, [query projection], decode, up-projection.
@@ -141,6 +195,9 @@ class DecodeStep:
         reads no cache row), so the append runs on a second stream beside it; the attention
         waits for both.  Under stream capture this becomes two branches of the graph.
         """
+        if self.n_q > 1:                        # the multi-query decode is one call
+            self.step_serial(stream)
+            return
         main = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(self.device)
         self.side.wait_stream(main)             # this step's inputs, and earlier reads of the cache
         self.append(self.side)
@@ -189,7 +246,8 @@ def from_workload(wl, ctx_lens=None, num_splits: int = 0, device: str = "cuda", 
         ctx_lens = mla_inputs.context_lengths(wl)
     st = DecodeStep(n_heads=wl.n_heads, d_h=wl.d_h, d_c=wl.d_c, d_r=wl.d_r, hidden=wl.hidden,
                     dtype=wl.dtype, ctx_lens=ctx_lens, n_new=wl.n_new, rope_base=wl.rope_base,
-                    query_from_h=wl.query_from_h, num_splits=num_splits, device=device)
+                    query_from_h=wl.query_from_h, d_q=wl.d_q, n_q=wl.n_q, num_splits=num_splits,
+                    device=device)
     if load_inputs:
         weights, h, queries = mla_inputs.make_all(wl)
         st.set_weights(weights)

@@ -120,6 +120,29 @@ MLA_API size_t mla_append_workspace_size(const mla_dims* dims, mla_dtype dtype, 
                                          int32_t n_new);
 
 /*
+ * mla_project_query_latent -- the query's own latent, c_q = W_DQ h ("Grouped-query and
+ * latent attention", section "Multi-head latent attention": the query is compressed
+ * like the keys and values, with a query latent of d_q = 1536 in DeepSeek-V3).
+ *
+ *   h      [batch, hidden]      the token inputs (one per sequence)
+ *   w_dq   [d_q, hidden]        query down-projection
+ *   workspace  device scratch of at least mla_query_latent_workspace_size(dims, dtype, batch,
+ *              d_q) bytes, 256-byte aligned (may be NULL when that size is 0); contents ignored
+ *   c_q    [batch, d_q]         out, rounded once from the fp32 accumulator to `dtype`
+ *   dev_status                  MLA_DEV_TIMEOUT if a bounded wait expired
+ * bf16 with d_q a multiple of 128 and hidden a multiple of 64 runs on tensor cores (the
+ * long hidden reduction split across CTAs, partial sums added in a fixed order).
+ */
+MLA_API mla_status mla_project_query_latent(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_q,
+                                    const void* h, const void* w_dq, void* workspace,
+                                    size_t workspace_bytes, void* c_q, int32_t* dev_status,
+                                    void* stream);
+
+/* Bytes of workspace mla_project_query_latent needs (0: none, or bad arguments). */
+MLA_API size_t mla_query_latent_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                               int32_t d_q);
+
+/*
  * mla_project_query -- per-head query parts from a query input x (the query latent
  * c_q, or h itself when the model has no query down-projection): q_C = W_UQ x and
  * q_R = W_QR x, the latter NOT yet rotated (decode rotates it at the query's
@@ -129,10 +152,13 @@ MLA_API size_t mla_append_workspace_size(const mla_dims* dims, mla_dtype dtype, 
  *   x     [batch, d_in]
  *   w_uq  [n_h*d_h, d_in]       w_qr [n_h*d_r, d_in]
  *   q_c   [batch, n_h, d_h]     q_r  [batch, n_h, d_r]
+ *   dev_status                  MLA_DEV_TIMEOUT if a bounded wait expired
+ * bf16 with n_h*d_h a multiple of 128, d_in a multiple of 64 and 16-byte aligned
+ * buffers runs both products in one tensor-core launch; other shapes on CUDA cores.
  */
 MLA_API mla_status mla_project_query(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t d_in,
                              const void* x, const void* w_uq, const void* w_qr,
-                             void* q_c, void* q_r, void* stream);
+                             void* q_c, void* q_r, int32_t* dev_status, void* stream);
 
 /*
  * mla_decode_workspace_size -- bytes of device workspace mla_decode_absorbed needs
@@ -178,6 +204,35 @@ MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, in
                                void* o_lat, float* lse, int32_t* dev_status, void* stream);
 
 /*
+ * mla_decode_absorbed_multi -- n_q causal queries per sequence (several new tokens decoded
+ * at once, as in a verification step of speculative decoding or a short chunk of prefill):
+ * query j of sequence b sits at position seq_len[b] - n_q + j and attends over rows
+ * 0 .. that position, with the absorption of mla_decode_absorbed ("Grouped-query and
+ * latent attention", section "The absorption trick"; the causal rule of "The Journey to
+ * Multi-Head Latent Attention", section "The KV cache": a token attends to itself and
+ * every earlier token).
+ *
+ *   q_c  [batch, n_q, n_h, d_h]    q_r [batch, n_q, n_h, d_r] (not yet rotated)
+ *   o_lat [batch, n_q, n_h, d_c]   lse [batch, n_q, n_h] (may be NULL)
+ *   workspace  at least mla_decode_multi_workspace_size(dims, dtype, batch, n_q, max_seq_len,
+ *              num_splits) bytes, 256-byte aligned
+ * Every other argument is as for mla_decode_absorbed.  Each query is decoded as a sequence
+ * of its own over the shared cache rows (the rows a chunk of queries shares are read once
+ * per query).  A query whose position would be negative (seq_len[b] < n_q) counts as an
+ * empty sequence: MLA_DEV_BAD_LENGTH, zero outputs, lse -inf.
+ */
+MLA_API mla_status mla_decode_absorbed_multi(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_q,
+                                     const void* q_c, const void* q_r, const void* w_uk,
+                                     const void* cache, int64_t cache_rows, const int64_t* row_off,
+                                     const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* o_lat, float* lse, int32_t* dev_status, void* stream);
+
+/* Bytes of workspace mla_decode_absorbed_multi needs (0 for arguments it would reject). */
+MLA_API size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                               int32_t n_q, int32_t max_seq_len, int32_t num_splits);
+
+/*
  * mla_decode_prepare, mla_decode_attend -- mla_decode_absorbed in two calls, so that the
  * query-side work can run beside the cache append of the same step (the fold reads no
  * cache row).  Both take exactly the arguments of mla_decode_absorbed, and the two calls
@@ -216,6 +271,54 @@ MLA_API mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_
                            void* stream);
 
 /*
+ * mla_project_output -- the attention layer's output u = W_O [o_1 ; ... ; o_n_h] after the
+ * per-head value up-projection (mla_project_out), the two-step form of "Grouped-query and
+ * latent attention", section "The absorption trick" (value side).
+ *
+ *   o     [batch, n_h, d_h]       per-head outputs (from mla_project_out)
+ *   w_o   [hidden, n_h*d_h]       output projection
+ *   u     [batch, hidden]         out, rounded once from the fp32 sums
+ *   workspace  at least mla_output_workspace_size(dims, dtype, batch, 0) bytes, 256-byte aligned
+ *   dev_status                    MLA_DEV_TIMEOUT if a bounded wait expired
+ * bf16 with d_h, d_c and hidden multiples of 128 (tensor cores); MLA_ERR_UNSUPPORTED otherwise.
+ */
+MLA_API mla_status mla_project_output(const mla_dims* dims, mla_dtype dtype, int32_t batch, const void* o,
+                              const void* w_o, void* workspace, size_t workspace_bytes, void* u,
+                              int32_t* dev_status, void* stream);
+
+/*
+ * mla_merge_output_weights -- W_UV merged into W_O ("Grouped-query and latent attention",
+ * section "The absorption trick": the value up-projection can be merged into the output
+ * matrix; "The Journey to Multi-Head Latent Attention", section "The absorption trick"):
+ * W_OV^(i) = W_O^(i) W_UV^(i), with W_O^(i) the columns i*d_h .. (i+1)*d_h - 1 of W_O.
+ * A one-time preparation of the weights.
+ *
+ *   w_o   [hidden, n_h*d_h]    w_uv [n_h, d_h, d_c]
+ *   w_ov  [n_h, d_c, hidden]   out: element (i, c, m) = sum_k W_O[m, i*d_h + k] W_UV[i, k, c]
+ * Same shape rule as mla_project_output.
+ */
+MLA_API mla_status mla_merge_output_weights(const mla_dims* dims, mla_dtype dtype, const void* w_o,
+                                    const void* w_uv, void* w_ov, int32_t* dev_status, void* stream);
+
+/*
+ * mla_project_output_merged -- u = sum_i W_OV^(i) o_lat_i straight from the decode's latent
+ * output (no per-head o), with the merged weights of mla_merge_output_weights.  It reads
+ * n_h*d_c*hidden weights instead of n_h*d_h*(d_c + hidden): for DeepSeek-V3 shapes
+ * (128 heads, d_h 128, d_c 512, hidden 7168) 939 MB against 252 MB in bf16, so the
+ * two-step form moves fewer bytes per decode step.
+ *
+ *   o_lat [batch, n_h, d_c]    w_ov [n_h, d_c, hidden]    u [batch, hidden]
+ *   workspace  at least mla_output_workspace_size(dims, dtype, batch, 1) bytes, 256-byte aligned
+ */
+MLA_API mla_status mla_project_output_merged(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                     const void* o_lat, const void* w_ov, void* workspace,
+                                     size_t workspace_bytes, void* u, int32_t* dev_status, void* stream);
+
+/* Bytes of workspace the output projection needs (merged != 0: the merged form). */
+MLA_API size_t mla_output_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                         int32_t merged);
+
+/*
  * mla_decode_absorbed_noalloc -- mla_decode_absorbed for callers that cannot allocate
  * device memory (code running where cudaMalloc is unavailable or not allowed, such as
  * inside an allocator's own callbacks or in hosts that hand out all device memory).
@@ -224,12 +327,12 @@ MLA_API mla_status mla_project_out(const mla_dims* dims, mla_dtype dtype, int32_
  * Same arguments and results as mla_decode_absorbed, minus the workspace: the scratch
  * is a fixed 32 MiB array compiled into the library, which every GPU that loads the
  * library keeps until the process exits.  Nothing is allocated or freed by the call.
- * - Returns MLA_ERR_WORKSPACE, before any CUDA call, when
+ * - Returns MLA_ERR_WORKSPACE, before any kernel launch or device memory access, when
  *   mla_decode_workspace_size(dims, dtype, batch, max_seq_len, num_splits) exceeds
  *   32 MiB (lower num_splits, batch or max_seq_len, or use mla_decode_absorbed).
- * - The first call on a device looks up that device's address of the array
- *   (cudaGetSymbolAddress, with the device current); make that first call before any
- *   stream capture.
+ * - Every call looks up the current device's address of the array
+ *   (cudaGetSymbolAddress); the first call on a device may load the library's GPU code
+ *   there, so make that first call before any stream capture.
  * - All calls on a device share the one array and it keeps the last call's contents
  *   (nothing in it needs clearing: the decode overwrites whatever it reads).  Calls
  *   whose work overlaps on the GPU (different streams, or host threads without
@@ -241,6 +344,18 @@ MLA_API mla_status mla_decode_absorbed_noalloc(const mla_dims* dims, mla_dtype d
                                        const int32_t* seq_len, int32_t max_seq_len,
                                        int32_t num_splits, void* o_lat, float* lse,
                                        int32_t* dev_status, void* stream);
+
+/*
+ * mla_set_wait_limit_ns -- time limit, in nanoseconds, of every bounded wait inside the
+ * pipelined tensor-core kernels (attention, projections) enqueued after this call by any
+ * host thread; 0 restores the default of 2 s.  Returns the previous limit.  A wait that
+ * runs out sets MLA_DEV_TIMEOUT in *dev_status; the kernel then stops issuing work, waits
+ * for its own copies and MMAs already in flight (those waits keep the 2 s bound), frees its
+ * tensor memory and returns, and the outputs of that call are undefined.  The default is
+ * far above the longest wait of a healthy launch; lowering it serves tests of the
+ * time-out path.  The library's own protocol, not a page of the method, defines it.
+ */
+MLA_API uint64_t mla_set_wait_limit_ns(uint64_t ns);
 
 /* Static description of a status code (never NULL). */
 MLA_API const char* mla_status_string(mla_status status);

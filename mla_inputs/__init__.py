@@ -9,9 +9,11 @@ Recipe (every draw uses ``torch.Generator('cpu')``):
 
 * One master generator seeded with the workload seed draws, in this order:
   the ragged context lengths (only for ragged workloads), ``W_DKV``, ``W_KR``,
-  ``W_UK``, ``W_UV``, ``W_UQ``/``W_QR`` (only when the query is projected from
-  ``h``), then ``h`` for the appended tokens, then ``q_C`` and ``q_R`` (only when
-  the query is drawn directly).
+  ``W_UK``, ``W_UV``, ``W_DQ`` (only when the query is projected from ``h`` through
+  a query latent), ``W_UQ``/``W_QR`` (only when the query is projected from ``h``),
+  then ``h`` for the appended tokens, then ``q_C`` and ``q_R`` (only when the query
+  is drawn directly), then ``W_O`` (only for workloads that include the output
+  projection).
 * The pre-filled latent rows of sequence ``b`` come from a generator of their
   own, seeded ``seed * 1_000_003 + 1 + b``, so any one sequence can be rebuilt
   without drawing the others.
@@ -56,8 +58,10 @@ class Workload:
     query_std: Optional[float] = None
     query_from_h: bool = False      # q_C = W_UQ h, q_R = W_QR h (no query down-projection given)
     ragged: Optional[tuple] = None  # (low, high) inclusive bounds for ragged context lengths
-    d_q: Optional[int] = None       # query latent width of the full model (not used by this path)
+    d_q: Optional[int] = None       # query latent width (c_q = W_DQ h) when the query comes from h
     rope_base: float = 10000.0
+    n_q: int = 1                    # causal queries per sequence (the last n_q new tokens)
+    w_o: bool = False               # also draw the output matrix W_O [hidden, n_h*d_h] (drawn last)
 
     @property
     def row_elems(self) -> int:
@@ -76,6 +80,11 @@ WORKLOADS = {
     "v3_b64_l4096": Workload("v3_b64_l4096", "bf16", batch=64, n_heads=128, d_h=128, d_c=512,
                              d_r=64, hidden=7168, prefill=4096, n_new=1, seed=2,
                              weight_std=0.02, d_q=1536),
+    # the same decode with the query computed from the new token's h: c_q = W_DQ h (query
+    # latent 1536), q_C = W_UQ c_q, q_R = W_QR c_q
+    "v3_b64_l4096_from_h": Workload("v3_b64_l4096_from_h", "bf16", batch=64, n_heads=128, d_h=128,
+                                    d_c=512, d_r=64, hidden=7168, prefill=4096, n_new=1, seed=2,
+                                    weight_std=0.02, d_q=1536, query_from_h=True),
     # long-context ragged decode: 16 sequences, context lengths uniform in [1024, 131072]
     "v3_ragged_b16": Workload("v3_ragged_b16", "bf16", batch=16, n_heads=128, d_h=128, d_c=512,
                               d_r=64, hidden=7168, prefill=None, n_new=1, seed=3,
@@ -138,20 +147,27 @@ def _draw_all(wl: Workload):
     w["w_uk"] = _normal(g, (wl.n_heads, wl.d_h, wl.d_c), _std(wl, wl.d_c), dt)
     w["w_uv"] = _normal(g, (wl.n_heads, wl.d_h, wl.d_c), _std(wl, wl.d_c), dt)
     if wl.query_from_h:
-        w["w_uq"] = _normal(g, (wl.n_heads * wl.d_h, wl.hidden), _std(wl, wl.hidden), dt)
-        w["w_qr"] = _normal(g, (wl.n_heads * wl.d_r, wl.hidden), _std(wl, wl.hidden), dt)
+        d_in = wl.hidden
+        if wl.d_q:
+            w["w_dq"] = _normal(g, (wl.d_q, wl.hidden), _std(wl, wl.hidden), dt)
+            d_in = wl.d_q
+        w["w_uq"] = _normal(g, (wl.n_heads * wl.d_h, d_in), _std(wl, d_in), dt)
+        w["w_qr"] = _normal(g, (wl.n_heads * wl.d_r, d_in), _std(wl, d_in), dt)
     h = _normal(g, (wl.batch, wl.n_new, wl.hidden), wl.act_std, dt)
     q = None
     if not wl.query_from_h:
         q_std = wl.act_std if wl.query_std is None else wl.query_std
-        q_c = _normal(g, (wl.batch, wl.n_heads, wl.d_h), q_std, dt)
-        q_r = _normal(g, (wl.batch, wl.n_heads, wl.d_r), q_std, dt)
+        lead = (wl.batch,) if wl.n_q == 1 else (wl.batch, wl.n_q)
+        q_c = _normal(g, lead + (wl.n_heads, wl.d_h), q_std, dt)
+        q_r = _normal(g, lead + (wl.n_heads, wl.d_r), q_std, dt)
         q = (q_c, q_r)
+    if wl.w_o:
+        w["w_o"] = _normal(g, (wl.hidden, wl.n_heads * wl.d_h), _std(wl, wl.n_heads * wl.d_h), dt)
     return w, h, q
 
 
 def make_weights(wl: Workload) -> dict:
-    """W_DKV [d_c,hidden], W_KR [d_r,hidden], W_UK/W_UV [n_h,d_h,d_c] (+ W_UQ, W_QR)."""
+    """W_DKV [d_c,hidden], W_KR [d_r,hidden], W_UK/W_UV [n_h,d_h,d_c] (+ W_DQ, W_UQ, W_QR)."""
     return _draw_all(wl)[0]
 
 
@@ -161,7 +177,8 @@ def make_tokens(wl: Workload) -> torch.Tensor:
 
 
 def make_queries(wl: Workload):
-    """(q_C [B,n_h,d_h], q_R [B,n_h,d_r]) drawn directly; None when projected from h."""
+    """(q_C [B,n_h,d_h], q_R [B,n_h,d_r]) drawn directly ([B,n_q,...] for several queries
+    per sequence); None when projected from h."""
     return _draw_all(wl)[2]
 
 

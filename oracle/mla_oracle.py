@@ -40,8 +40,8 @@ import numpy as np
 __all__ = [
     "f64", "round_to_bf16", "rope_inverse_frequencies", "rope", "append_rows",
     "expand_heads", "full_keys", "decode_explicit", "decode_absorbed",
-    "project_query", "project_out", "softmax_scale", "cache_elements_per_token",
-    "cache_bytes",
+    "project_query", "project_out", "project_output", "merge_output_weights",
+    "project_output_merged", "softmax_scale", "cache_elements_per_token", "cache_bytes",
 ]
 
 
@@ -240,6 +240,27 @@ def project_query(x, w_uq, w_qr, n_h: int, w_dq=None):
 def project_out(o_lat, w_uv) -> np.ndarray:
     """o_i = W_UV^(i) o_lat_i for every head: [..., n_h, d_c] -> [..., n_h, d_h]."""
     return np.einsum("hdc,...hc->...hd", f64(w_uv), f64(o_lat))
+
+
+def project_output(o, w_o) -> np.ndarray:
+    """The layer output u = W_O [o_1 ; ... ; o_n_h]: the heads' outputs side by side, then
+    the output matrix.  o [..., n_h, d_h], W_O [hidden, n_h*d_h] -> u [..., hidden]."""
+    o = f64(o)
+    return o.reshape(*o.shape[:-2], -1) @ f64(w_o).T
+
+
+def merge_output_weights(w_o, w_uv) -> np.ndarray:
+    """W_UV merged into W_O ("Grouped-query and latent attention", section "The absorption
+    trick"): W_OV^(i) = W_O^(i) W_UV^(i), W_O^(i) being the d_h columns of head i.
+    W_O [hidden, n_h*d_h], W_UV [n_h, d_h, d_c] -> [n_h, hidden, d_c]."""
+    w_o, w_uv = f64(w_o), f64(w_uv)
+    n_h, d_h, _ = w_uv.shape
+    return np.stack([w_o[:, i * d_h:(i + 1) * d_h] @ w_uv[i] for i in range(n_h)])
+
+
+def project_output_merged(o_lat, w_ov) -> np.ndarray:
+    """u = sum_i W_OV^(i) o_lat_i: o_lat [..., n_h, d_c], W_OV [n_h, hidden, d_c]."""
+    return np.einsum("hmc,...hc->...m", f64(w_ov), f64(o_lat))
 
 
 def cache_elements_per_token(kind: str, *, n_h: int = 0, d_h: int = 0, n_g: int = 0,

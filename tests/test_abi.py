@@ -69,8 +69,13 @@ def test_null_pointers_rejected_on_host():
                   1 << 20, fake, None, fake, None) == mla.MLA_ERR_INVALID_ARG
         assert fn(ctypes.byref(d), 0, 1, fake, fake, fake, fake, 64, fake, fake, 8, 1, None,
                   1 << 20, fake, None, fake, None) == mla.MLA_ERR_WORKSPACE
-    assert lib.mla_project_query(ctypes.byref(d), 0, 1, 64, fake, fake, None, fake, fake,
+    assert lib.mla_project_query(ctypes.byref(d), 0, 1, 64, fake, fake, None, fake, fake, fake,
                                  None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_project_query(ctypes.byref(d), 0, 1, 64, fake, fake, fake, fake, fake, None,
+                                 None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_project_query_latent(ctypes.byref(d), 0, 1, 32, fake, None, None, 0, fake, fake,
+                                        None) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_query_latent_workspace_size(ctypes.byref(d), 0, 1, 32) == 0
     assert lib.mla_cache_append(None, 0, 1, 1, fake, fake, fake, fake, fake, fake, fake, 64, None, 0, fake,
                                 None) == mla.MLA_ERR_INVALID_ARG
 

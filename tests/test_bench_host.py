@@ -40,3 +40,16 @@ def test_fp32_rows_count_four_bytes():
 
 def test_job_throughput_counts_every_rank():
     assert bench.job_throughput(64, 8, 1000, 150.0) == pytest.approx(64 * 8 * 1000 / 0.150)
+
+
+def test_clock_summary_keeps_only_samples_inside_the_windows():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.period, cs.error, cs.source = 0.002, None, "nvml"
+    cs.rows = [(1.0, 1000.0, 2032.0, 0), (2.0, 2032.0, 2032.0, 0x4), (2.5, 1900.0, 2032.0, 0),
+               (3.0, 500.0, 2032.0, 0x40 | 0x8)]
+    s = cs.summary([(1.9, 2.6)])
+    assert s["samples"] == 2 and s["sm_mhz"] == 1966.0 and s["reasons"] == ["sw_power_cap"]
+    s = cs.summary([(0.5, 1.5), (2.9, 3.1)])
+    assert s["samples"] == 2 and s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    s = cs.summary([(5.0, 6.0)])
+    assert s["samples"] == 0 and s["sm_mhz"] is None and s["error"]

@@ -191,6 +191,45 @@ def pin_query_and_out_projections():
     assert np.array_equal(q_r, [[-1, 0], [-2, 0]])
 
 
+def pin_query_latent_projection():
+    """With a query down-projection the query parts come from c_q = W_DQ h ("Grouped-query
+    and latent attention", section "Multi-head latent attention"): here W_DQ picks h_0 and
+    h_2, so c_q = [1, 3]; W_UQ (2 heads of width 1) and W_QR (2 heads of width 2) are
+    integer matrices with hand-computed products."""
+    h = np.array([1.0, 7.0, 3.0, -5.0])
+    w_dq = np.array([[1.0, 0.0, 0.0, 0.0], [0.0, 0.0, 1.0, 0.0]])
+    w_uq = np.array([[1.0, 0.0], [0.0, 2.0]])
+    w_qr = np.array([[1.0, 1.0], [0.0, 1.0], [2.0, 0.0], [0.0, 0.0]])
+    q_c, q_r = mo.project_query(h, w_uq, w_qr, 2, w_dq=w_dq)
+    assert np.array_equal(q_c, [[1.0], [6.0]])
+    assert np.array_equal(q_r, [[4.0, 3.0], [2.0, 0.0]])
+    # a batch of tokens is projected row by row
+    q_c2, q_r2 = mo.project_query(np.stack([h, 2 * h]), w_uq, w_qr, 2, w_dq=w_dq)
+    assert np.array_equal(q_c2[1], 2 * q_c) and np.array_equal(q_r2[1], 2 * q_r)
+
+
+def pin_output_projection_and_merge():
+    """u = W_O [o_1; o_2] with the worked example's value projections; W_UV merged into W_O
+    gives the same u straight from the latents (hand-computed integers), and the merged
+    and two-step forms agree on random shapes."""
+    g, _, w_uv = _worked_example_weights()                # 2 heads, d_h 2, d_c 3
+    c = np.array(g["c"], float)                           # [1, 2, 3]
+    w_o = np.array([[1.0, 0.0, 0.0, 1.0], [0.0, 2.0, 1.0, 0.0]])   # hidden 2, n_h*d_h 4
+    o = mo.project_out(np.array([c, c]), w_uv)            # [[4, 2], [1, 5]]
+    u = mo.project_output(o, w_o)
+    assert np.array_equal(u, [4 + 5, 2 * 2 + 1])
+    w_ov = mo.merge_output_weights(w_o, w_uv)
+    assert w_ov.shape == (2, 2, 3)
+    assert np.array_equal(mo.project_output_merged(np.array([c, c]), w_ov), u)
+    rng = np.random.default_rng(5)
+    w_o = rng.normal(size=(6, 3 * 4))
+    w_uv = rng.normal(size=(3, 4, 5))
+    o_lat = rng.normal(size=(2, 3, 5))
+    two_step = mo.project_output(mo.project_out(o_lat, w_uv), w_o)
+    merged = mo.project_output_merged(o_lat, mo.merge_output_weights(w_o, w_uv))
+    assert np.allclose(two_step, merged, rtol=0, atol=1e-12)
+
+
 def pin_bf16_rounding():
     """The cache's bf16 rounding equals torch's round-to-nearest-even conversion."""
     rng = np.random.default_rng(0)
@@ -241,7 +280,8 @@ def pin_scale():
 ALL_PINS = [pin_worked_example_heads, pin_full_key_concat, pin_single_row_decode,
             pin_two_rows_content, pin_rotary_query_position, pin_identical_rows,
             pin_dominant_row, pin_absorption_invariant, pin_rope_closed_forms,
-            pin_append_closed_form, pin_query_and_out_projections, pin_bf16_rounding,
+            pin_append_closed_form, pin_query_and_out_projections, pin_query_latent_projection,
+            pin_output_projection_and_merge, pin_bf16_rounding,
             pin_cache_tables, pin_scale]
 
 
