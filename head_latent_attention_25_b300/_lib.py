@@ -23,13 +23,21 @@ EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size"
             "mla_decode_prepare", "mla_decode_attend", "mla_set_wait_limit_ns",
             "mla_project_query_latent", "mla_query_latent_workspace_size",
             "mla_decode_absorbed_multi", "mla_decode_multi_workspace_size", "mla_project_output",
-            "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size")
+            "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size",
+            "mla_cache_append_ex", "mla_decode_absorbed_ex")
 
 
 class MlaDims(ctypes.Structure):
     _fields_ = [("n_heads", ctypes.c_int32), ("d_h", ctypes.c_int32), ("d_c", ctypes.c_int32),
                 ("d_r", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("rope_base", ctypes.c_float), ("softmax_scale", ctypes.c_float)]
+
+
+class MlaCacheLayout(ctypes.Structure):
+    """mla_cache_layout: where the latent rows live (packed or split, contiguous or paged)."""
+    _fields_ = [("kv", ctypes.c_void_p), ("pe", ctypes.c_void_p), ("kv_stride", ctypes.c_int64),
+                ("pe_stride", ctypes.c_int64), ("rows", ctypes.c_int64), ("block_table", ctypes.c_void_p),
+                ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32)]
 
 
 class MlaError(RuntimeError):
@@ -71,6 +79,11 @@ def load():
     lib.mla_decode_absorbed_multi.restype = I32
     lib.mla_decode_multi_workspace_size.argtypes = [D, I32, I32, I32, I32, I32]
     lib.mla_decode_multi_workspace_size.restype = SZ
+    CL = ctypes.POINTER(MlaCacheLayout)
+    lib.mla_cache_append_ex.argtypes = [D, I32, I32, I32, P, P, P, CL, P, P, P, P, SZ, P, P]
+    lib.mla_cache_append_ex.restype = I32
+    lib.mla_decode_absorbed_ex.argtypes = [D, I32, I32, P, P, P, CL, P, P, I32, I32, P, SZ, P, P, P, P]
+    lib.mla_decode_absorbed_ex.restype = I32
     lib.mla_project_output.argtypes = [D, I32, I32, P, P, P, SZ, P, P, P]
     lib.mla_project_output.restype = I32
     lib.mla_project_output_merged.argtypes = [D, I32, I32, P, P, P, SZ, P, P, P]
@@ -265,3 +278,28 @@ def mla_project_output_merged(dims, dtype, batch, o_lat, w_ov, workspace, worksp
     _check("mla_project_output_merged", load().mla_project_output_merged(
         ctypes.byref(dims), dtype, batch, _p(o_lat), _p(w_ov), _p(workspace), workspace_bytes, _p(u),
         _p(dev_status), _stream(stream)))
+
+
+def make_cache_layout(kv, pe=None, kv_stride=None, pe_stride=None, rows=None, block_table=None,
+                      block_size=0, max_blocks=0) -> MlaCacheLayout:
+    """An mla_cache_layout from tensors (strides and rows default to the tensors' own)."""
+    return MlaCacheLayout(_p(kv), _p(pe), kv_stride if kv_stride is not None else kv.shape[-1],
+                          (pe_stride if pe_stride is not None else pe.shape[-1]) if pe is not None else 0,
+                          rows if rows is not None else kv.shape[0], _p(block_table), block_size, max_blocks)
+
+
+def mla_cache_append_ex(dims, dtype, batch, n_new, h, w_dkv, w_kr, layout, row_off, cap, pos0, workspace,
+                        workspace_bytes, dev_status, stream=None):
+    """mla_cache_append into the cache described by ``layout`` (an MlaCacheLayout)."""
+    _check("mla_cache_append_ex", load().mla_cache_append_ex(
+        ctypes.byref(dims), dtype, batch, n_new, _p(h), _p(w_dkv), _p(w_kr), ctypes.byref(layout), _p(row_off),
+        _p(cap), _p(pos0), _p(workspace), workspace_bytes, _p(dev_status), _stream(stream)))
+
+
+def mla_decode_absorbed_ex(dims, dtype, batch, q_c, q_r, w_uk, layout, row_off, seq_len, max_seq_len,
+                           num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream=None):
+    """mla_decode_absorbed over the cache described by ``layout`` (an MlaCacheLayout)."""
+    _check("mla_decode_absorbed_ex", load().mla_decode_absorbed_ex(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), ctypes.byref(layout), _p(row_off),
+        _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes, _p(o_lat), _p(lse), _p(dev_status),
+        _stream(stream)))

@@ -174,8 +174,9 @@ mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32_t batch
         const size_t need = append_tc_workspace(*dims, batch * n_new, nullptr, sms);
         if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
         if (!aligned(h, 16) || !aligned(w_dkv, 16) || !aligned(w_kr, 16)) return MLA_ERR_INVALID_ARG;
+        const CacheView cv{cache, nullptr, dims->d_c + dims->d_r, 0, cache_rows, nullptr, 0, 0};
         return cuda_status(launch_append_tc(*dims, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0,
-                                            cache, cache_rows, workspace, dev_status, sms, s));
+                                            cv, workspace, dev_status, sms, s));
     }
     return cuda_status(launch_append(*dims, dtype == MLA_BF16, batch, n_new, h, w_dkv, w_kr,
                                      row_off, cap, pos0, cache, cache_rows, dev_status, s));
@@ -298,20 +299,26 @@ enum : int { kPrepare = 1, kAttend = 2 };
 
 // The decode in two phases: kPrepare (fold W_UK^T into the queries, rotate q_R, build the
 // schedule; reads no cache row) and kAttend (split-K attention over the cache, merge).
+// `layout` (null: the packed contiguous cache `cache`) selects where the rows live; a
+// layout other than packed contiguous runs on the tensor-core kernel only.
 mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int32_t batch,
                          const void* q_c, const void* q_r, const void* w_uk,
                          const void* cache, int64_t cache_rows, const int64_t* row_off,
                          const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
                          void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
-                         int32_t* dev_status, void* stream) {
+                         int32_t* dev_status, void* stream, const CacheView* layout = nullptr) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || max_seq_len < 0 || num_splits < 0 || cache_rows < 1) return MLA_ERR_INVALID_ARG;
-    if (!q_c || !q_r || !w_uk || !cache || !row_off || !seq_len || !o_lat || !dev_status)
+    if (!q_c || !q_r || !w_uk || !cache || (!row_off && !(layout && layout->block_table)) || !seq_len ||
+        !o_lat || !dev_status)
         return MLA_ERR_INVALID_ARG;
     const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
     const bool tc = tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
     if (!tc && !simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
+    if (layout && !tc) return MLA_ERR_UNSUPPORTED;
+    CacheView cv{cache, nullptr, dims->d_c + dims->d_r, 0, cache_rows, nullptr, 0, 0};
+    if (layout) cv = *layout;
     DecodePlan p;
     if (!plan_decode(dims, dtype, batch, max_seq_len, num_splits, tc, &p)) return MLA_ERR_CUDA;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < p.ws.total)
@@ -327,8 +334,10 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
     const bool bf16 = dtype == MLA_BF16;
     const float alpha = scale_of(dims) * kLog2e;
     cudaError_t e = cudaSuccess;
+    // a paged cache flattens the context in whole tiles, so no tile crosses a block
     const ScheduleArgs sa{seq_len, row_off, cache_rows, batch, p.workers, cum, (Schedule*)sched, wstart,
-                          dev_status};
+                          dev_status, cv.block_table ? 64 : 1,
+                          cv.block_table ? (int64_t)cv.max_blocks * cv.block_size : 0};
     if (phases & kPrepare) {
         if (tc && gemm_tc_shapes_ok(*dims) && aligned(q_c, 16) && aligned(w_uk, 16)) {
             // fold GEMM, then q_R rotation and the schedule in one launch
@@ -346,7 +355,7 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
         if (tc) {
             // when this call also ran the prepare kernels, the attention kernel may start
             // (set-up only) before the last of them ends
-            e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cache, cache_rows, row_off, cum,
+            e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cv, seq_len, row_off, cum,
                                 sched, wstart, o_lat, lse, part_o, part_l, dev_status, s,
                                 (phases & kPrepare) != 0);
         } else {
@@ -417,6 +426,54 @@ mla_status mla_decode_absorbed_multi(const mla_dims* dims, mla_dtype dtype, int3
     return decode_phases(kPrepare | kAttend, dims, dtype, (int32_t)nv, q_c, q_r, w_uk, cache, cache_rows, row_off_v,
                          seq_len_v, max_seq_len, num_splits, (char*)workspace + idx, workspace_bytes - idx, o_lat,
                          lse, dev_status, stream);
+}
+
+// Checks a caller's cache layout for the tensor-core shapes (d_c = 512, d_r = 64) and
+// turns it into the internal view.
+static mla_status view_of(const mla_dims* d, const mla_cache_layout* c, CacheView* v) {
+    if (!c || !c->kv || c->rows < 32 || c->rows > INT32_MAX) return MLA_ERR_INVALID_ARG;
+    const int64_t kv_need = c->pe ? d->d_c : d->d_c + d->d_r;
+    if (c->kv_stride < kv_need || c->kv_stride % 8 || !aligned(c->kv, 16)) return MLA_ERR_INVALID_ARG;
+    if (c->pe && (c->pe_stride < d->d_r || c->pe_stride % 8 || !aligned(c->pe, 16))) return MLA_ERR_INVALID_ARG;
+    if (c->block_table && (c->block_size < 64 || c->block_size % 64 || c->max_blocks < 1))
+        return MLA_ERR_INVALID_ARG;
+    *v = CacheView{c->kv, c->pe, c->kv_stride, c->pe ? c->pe_stride : 0, c->rows, c->block_table,
+                   c->block_table ? c->block_size : 0, c->block_table ? c->max_blocks : 0};
+    return MLA_OK;
+}
+
+mla_status mla_cache_append_ex(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
+                               const void* h, const void* w_dkv, const void* w_kr, const mla_cache_layout* cache,
+                               const int64_t* row_off, const int32_t* cap, const int32_t* pos0, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30)) return MLA_ERR_INVALID_ARG;
+    if (!h || !w_dkv || !w_kr || !cap || !pos0 || !dev_status) return MLA_ERR_INVALID_ARG;
+    if (!tc_shape(dims, dtype) || !gemm_tc_shapes_ok(*dims)) return MLA_ERR_UNSUPPORTED;
+    CacheView cv;
+    const mla_status st = view_of(dims, cache, &cv);
+    if (st != MLA_OK) return st;
+    if (!cv.block_table && !row_off) return MLA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    const size_t need = append_tc_workspace(*dims, batch * n_new, nullptr, sms);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    if (!aligned(h, 16) || !aligned(w_dkv, 16) || !aligned(w_kr, 16)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_append_tc(*dims, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cv, workspace,
+                                        dev_status, sms, (cudaStream_t)stream));
+}
+
+mla_status mla_decode_absorbed_ex(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                  const void* q_c, const void* q_r, const void* w_uk, const mla_cache_layout* cache,
+                                  const int64_t* row_off, const int32_t* seq_len, int32_t max_seq_len,
+                                  int32_t num_splits, void* workspace, size_t workspace_bytes, void* o_lat,
+                                  float* lse, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (!tc_shape(dims, dtype)) return MLA_ERR_UNSUPPORTED;
+    CacheView cv;
+    const mla_status st = view_of(dims, cache, &cv);
+    if (st != MLA_OK) return st;
+    return decode_phases(kPrepare | kAttend, dims, dtype, batch, q_c, q_r, w_uk, cv.kv, cv.rows, row_off, seq_len,
+                         max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream, &cv);
 }
 
 mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t batch,

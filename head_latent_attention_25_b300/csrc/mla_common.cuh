@@ -95,6 +95,25 @@ __host__ __device__ __forceinline__ void worker_range(const Schedule& S, const i
     }
 }
 
+// Where the latent rows of the cache live (the tensor-core path): the latent part in kv,
+// the rotary part in pe (or packed after the latent in kv), and the row of position t of
+// sequence b either row_off[b] + t (contiguous) or from a block table (paged).
+struct CacheView {
+    const void* kv;
+    const void* pe;                 // null: packed, the rotary part at column d_c of kv
+    int64_t kv_stride, pe_stride;   // elements between rows
+    int64_t rows;
+    const int32_t* block_table;     // null: contiguous
+    int32_t block_size, max_blocks;
+};
+
+// Row of position pos of sequence b (contiguous: row_off[b] + pos).
+__device__ __forceinline__ int64_t cache_row(const CacheView& c, const int64_t* row_off, int b, int64_t pos) {
+    if (!c.block_table) return row_off[b] + pos;
+    return (int64_t)c.block_table[(int64_t)b * c.max_blocks + pos / c.block_size] * c.block_size +
+           pos % c.block_size;
+}
+
 // Layout of the decode workspace (offsets in bytes, each 256-aligned).
 struct DecodeWorkspace {
     size_t q_off, q_bytes;          // folded query Q' [batch, n_h, d_c + d_r]

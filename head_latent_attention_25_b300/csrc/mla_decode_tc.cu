@@ -93,6 +93,10 @@ constexpr uint32_t kColS = 384;        // S[2] (by tile parity): 2 x 64 fp32 col
 struct TcArgs {
     const __nv_bfloat16* qp;           // folded queries [batch * n_h, 576]
     const int64_t* row_off;
+    const int32_t* seq_len;            // real lengths when the schedule pads sequences to whole tiles, else null
+    const int32_t* block_table;        // paged cache (null: contiguous, row_off)
+    int32_t block_size, max_blocks;
+    int32_t rope_x0;                   // column of the rotary part in its tensor map (512 packed, 0 split)
     const int64_t* cum;
     const Schedule* sched;
     const int32_t* wstart;             // first sequence of each worker's range
@@ -115,14 +119,21 @@ struct Seg {
 
 // Walks the sequences that a worker's range of the flattened context touches
 // (identical in every role of both CTAs).
+// kTiled: the context is flattened in whole tiles (a paged cache), so a sequence spans
+// its length rounded up to a tile and its real length comes from real_len; the rows past
+// its length are never visited (range boundaries are tile-aligned).  A separate
+// instantiation keeps the contiguous walk free of that work.
+template <bool kTiled>
 struct SegWalk {
     const int64_t* cum;
+    const int32_t* real_len;
     int64_t cur, end;
     int b, g;
     bool first;
     // start: the worker's first sequence, found by the schedule kernel
-    __device__ void init(const int64_t* c, int start, int gi, const Schedule& S) {
+    __device__ void init(const int64_t* c, const int32_t* rl, int start, int gi, const Schedule& S) {
         cum = c;
+        real_len = rl;
         g = gi;
         worker_range(S, c, gi, &cur, &end);
         first = true;
@@ -131,14 +142,14 @@ struct SegWalk {
     __device__ bool next(Seg& s) {
         if (cur >= end) return false;
         while (cum[b + 1] <= cur) ++b;
-        const int64_t seq0 = cum[b];
+        const int64_t seq0 = cum[b], span = cum[b + 1] - seq0;
         s.b = b;
-        s.len = cum[b + 1] - seq0;
+        s.len = kTiled ? min(span, (int64_t)real_len[b]) : span;
         s.lo = cur - seq0;
         s.hi = min(s.len, end - seq0);
         s.complete = (s.lo == 0 && s.hi == s.len);
         s.slot = 2 * (int64_t)g + (first ? 0 : 1);
-        cur = seq0 + s.hi;
+        cur = (kTiled && s.hi == s.len) ? seq0 + span : seq0 + s.hi;
         first = false;
         return true;
     }
@@ -147,8 +158,9 @@ struct SegWalk {
 __device__ __forceinline__ int tiles_of(const Seg& s) { return (int)((s.hi - s.lo + kTok - 1) / kTok); }
 
 // The worker's tiles in order: global tile index T, piece index si, tile t of ntiles.
+template <bool kTiled>
 struct TileIt {
-    SegWalk walk;
+    SegWalk<kTiled> walk;
     Seg seg;
     int t = -1, ntiles = 0;
     uint32_t T = 0xffffffffu, si = 0xffffffffu;
@@ -218,6 +230,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+template <bool kTiled>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
                 TcArgs a) {
@@ -293,10 +306,19 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             // the peer's partial arrives on a local barrier; this thread, which has no remote
             // stores of its own in flight, makes the cluster-scope release arrival).
             if (lane == 0) {
-                TileIt ip, ic;                              // next tile to load, next credit
-                ip.walk.init(a.cum, a.wstart[g], g, S);
-                ic.walk.init(a.cum, a.wstart[g], g, S);
+                TileIt<kTiled> ip, ic;                              // next tile to load, next credit
+                ip.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                ic.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 bool mp = ip.next(), mc = ic.next();
+                // cache row of the next tile to load, fetched one tile ahead (a block-table
+                // entry is a global load; its latency hides behind the wait for a free stage)
+                auto tile_row = [&](const TileIt<kTiled>& t) -> int {
+                    const int64_t pos = t.seg.lo + (int64_t)t.t * kTok;
+                    if (!kTiled) return (int)(a.row_off[t.seg.b] + pos);      // contiguous
+                    return a.block_table[(int64_t)t.seg.b * a.max_blocks + pos / a.block_size] * a.block_size +
+                           (int)(pos % a.block_size);
+                };
+                int next_y = mp ? tile_row(ip) : 0;
                 uint32_t issued = 0;
                 uint64_t t_prog = globaltimer_ns();
                 while (mp || mc) {
@@ -305,13 +327,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         const uint32_t T = ip.T, st = T % kStages;
                         if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
                             const uint32_t dst = sStage + st * kStageBytes;
-                            const int y = (int)(a.row_off[ip.seg.b] + ip.seg.lo + (int64_t)ip.t * kTok);
+                            const int y = next_y;
                             mbar_expect_tx(bar(B_FULL + st), kStageBytes);
                             for (int j = 0; j < 4; ++j)
                                 tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
-                            tma_load_2d(dst + 4 * kTBox, &map_c64, 512 + rank * kRopeHalf, y, bar(B_FULL + st));
+                            tma_load_2d(dst + 4 * kTBox, &map_c64, a.rope_x0 + rank * kRopeHalf, y, bar(B_FULL + st));
                             issued = T + 1;
                             mp = ip.next();
+                            if (mp) next_y = tile_row(ip);
                             prog = true;
                         }
                     }
@@ -351,8 +374,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 const uint32_t par = warp == 1 ? 0u : 1u;
                 const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
                 const uint32_t sQR = base + kOffQR;
-                TileIt it;
-                it.walk.init(a.cum, a.wstart[g], g, S);
+                TileIt<kTiled> it;
+                it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 bool ok = true;
                 while (ok && it.next()) {
                     const uint32_t T = it.T;
@@ -384,8 +407,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             if (lane == 0) {
                 const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
                 const uint32_t sP = base + kOffP;
-                TileIt it;
-                it.walk.init(a.cum, a.wstart[g], g, S);
+                TileIt<kTiled> it;
+                it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 bool ok = true;
                 while (ok && it.next()) {
                     const uint32_t T = it.T, st = T % kStages;
@@ -418,8 +441,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const uint32_t peer_x = mapa(sX + xb * kXBytes, peer);
             const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
                 float* mshare = (float*)(sm + kOffMh);
-            TileIt co;
-            co.walk.init(a.cum, a.wstart[g], g, S);
+            TileIt<kTiled> co;
+            co.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
             bool ok = true;
             float m_g = -INFINITY, l_g = 0.f;
             while (ok && co.next()) {
@@ -571,8 +594,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             reg_alloc_dec<96>();
             const int i = tid - 384;                        // head row == TMEM lane
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            SegWalk walk;
-            walk.init(a.cum, a.wstart[g], g, S);
+            SegWalk<kTiled> walk;
+            walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
             Seg cur, nxt;
             bool have = walk.next(cur);
             uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
@@ -693,10 +716,10 @@ bool get_encoder() {
     return g_encode != nullptr;
 }
 
-bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t bx, uint32_t by,
-               CUtensorMapSwizzle sw) {
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t stride, uint32_t bx,
+               uint32_t by, CUtensorMapSwizzle sw) {
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
+    cuuint64_t strides[1] = {stride * 2};
     cuuint32_t box[2] = {bx, by};
     cuuint32_t es[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
@@ -717,13 +740,13 @@ int resident_pairs() {
     std::lock_guard<std::mutex> lock(mu);
     if (cache[dev] == 0) {
         int n = 0;
-        if (cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+        if (cudaFuncSetAttribute(split_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
             cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 256);
             cfg.blockDim = dim3(kThreads);
             cfg.dynamicSmemBytes = kSmemBytes;
-            if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel<false>, &cfg) != cudaSuccess) n = 0;
         }
         (void)cudaGetLastError();
         cache[dev] = n > 0 ? n : -1;
@@ -742,23 +765,28 @@ int tc_workers(int64_t max_total_rows, int sm_count) {
 }
 
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
-                            int64_t q_rows, const void* cache, int64_t cache_rows,
+                            int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             const int32_t* wstart, void* o_lat, float* lse, float* part_o,
                             float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl) {
     (void)q_rows;
     if (!get_encoder()) return cudaErrorNotSupported;
+    // latent boxes from kv; the rotary box from pe, or from kv after the latent when packed
     CUtensorMap mc128, mc64;
-    if (!encode_2d(&mc128, cache, kRowElems, (uint64_t)cache_rows, 64, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&mc64, cache, kRowElems, (uint64_t)cache_rows, 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint64_t kv_cols = cv.pe ? 512 : (uint64_t)kRowElems;
+    if (!encode_2d(&mc128, cv.kv, kv_cols, (uint64_t)cv.rows, (uint64_t)cv.kv_stride, 64, kTok,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&mc64, cv.pe ? cv.pe : cv.kv, cv.pe ? 64 : (uint64_t)kRowElems, (uint64_t)cv.rows,
+                   (uint64_t)(cv.pe ? cv.pe_stride : cv.kv_stride), 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
-    TcArgs a{(const __nv_bfloat16*)qp, row_off, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
+    TcArgs a{(const __nv_bfloat16*)qp, row_off, cv.block_table ? seq_len : nullptr, cv.block_table,
+             cv.block_size, cv.max_blocks, cv.pe ? 0 : 512, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
              lse, part_o, part_l, dev_status, wait_limit_ns(), d.n_heads, batch};
-    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kernel = cv.block_table ? split_tc_kernel<true> : split_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     profile_before_split(s);
-    e = launch_ex(split_tc_kernel, dim3(2 * workers), dim3(kThreads), kSmemBytes, s, pdl, mc128, mc64, a);
+    e = launch_ex(kernel, dim3(2 * workers), dim3(kThreads), kSmemBytes, s, pdl, mc128, mc64, a);
     profile_after_split(s);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kFinPairs * kFinGroups)
 append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, int n_new, int d_c,
                        int d_r, double rope_r, const int64_t* __restrict__ row_off,
                        const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
-                       int64_t cache_rows, __nv_bfloat16* __restrict__ cache, int32_t* dev_status) {
+                       CacheView cv, int32_t* dev_status) {
     __shared__ float2 red[kFinGroups][kFinPairs];
     pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
     const int t = blockIdx.x;
@@ -283,9 +283,25 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
     const int e = 2 * (blockIdx.y * kFinPairs + x);
     const int b = t / n_new, j = t % n_new;
     const int p0 = pos0[b];
-    const int64_t off = row_off[b], cp = cap[b];
-    if (p0 < 0 || (int64_t)p0 + n_new > cp || off < 0 || off + cp > cache_rows) {
-        if (j == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
+    const int64_t cp = cap[b];
+    // contiguous: the sequence's rows must lie in the buffer; paged: its positions must be
+    // covered by its block-table entries, and this token's block must lie in the buffer
+    bool bad = p0 < 0 || (int64_t)p0 + n_new > cp;
+    int64_t row = -1;
+    if (!bad) {
+        if (!cv.block_table) {
+            const int64_t off = row_off[b];
+            bad = off < 0 || off + cp > cv.rows;
+        } else {
+            bad = cp > (int64_t)cv.max_blocks * cv.block_size;
+        }
+        if (!bad) {
+            row = cache_row(cv, row_off, b, (int64_t)p0 + j);
+            bad = row < 0 || row >= cv.rows;
+        }
+    }
+    if (bad) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
         return;
     }
     float2 acc = make_float2(0.f, 0.f);
@@ -317,7 +333,9 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
         v0 = r0;
         v1 = r1;
     }
-    *(__nv_bfloat162*)(cache + (off + pos) * width + e) = __floats2bfloat162_rn(v0, v1);
+    __nv_bfloat16* dst = (cv.pe && e >= d_c) ? (__nv_bfloat16*)cv.pe + row * cv.pe_stride + (e - d_c)
+                                             : (__nv_bfloat16*)cv.kv + row * cv.kv_stride + e;
+    *(__nv_bfloat162*)dst = __floats2bfloat162_rn(v0, v1);
 }
 
 // y[t, e] = bf16(sum over splits of part[split, t, e]) for a split-K GEMM, summed in a
@@ -605,7 +623,7 @@ cudaError_t launch_project_query_tc(const mla_dims& d, int batch, int d_in, cons
 
 cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
                              const void* w_kr, const int64_t* row_off, const int32_t* cap,
-                             const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                             const int32_t* pos0, const CacheView& cv, void* workspace,
                              int32_t* dev_status, int sm_count, cudaStream_t s) {
     if (!encoder()) return cudaErrorNotSupported;
     const int n_tok = batch * n_new;
@@ -637,7 +655,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
     const dim3 fin_grid(n_tok, (width / 2 + kFinPairs - 1) / kFinPairs);
     e = launch_ex(append_finalize_kernel, fin_grid, dim3(kFinPairs * kFinGroups), 0, s, true,
                   (const float*)workspace, splits, n_tok, n_new, d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
-                  row_off, cap, pos0, cache_rows, (__nv_bfloat16*)cache, dev_status);
+                  row_off, cap, pos0, cv, dev_status);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -42,9 +42,10 @@ cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int
 // tcgen05 projections (bf16; shapes accepted by gemm_tc_shapes_ok)
 bool gemm_tc_shapes_ok(const mla_dims& d);
 size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count);
+struct CacheView;
 cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
                              const void* w_kr, const int64_t* row_off, const int32_t* cap,
-                             const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                             const int32_t* pos0, const CacheView& cv, void* workspace,
                              int32_t* dev_status, int sm_count, cudaStream_t s);
 size_t query_latent_tc_workspace(int hidden, int d_q, int n_tok, int* k_splits_out, int sm_count);
 // c_q = W_DQ h on tensor cores (split-K GEMM, then a fixed-order reduction to bf16)
@@ -86,7 +87,7 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
 
 // bf16 tcgen05 split kernel for d_c = 512, d_r = 64, n_heads <= 128 (2-CTA clusters).
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
-                            int64_t q_rows, const void* cache, int64_t cache_rows,
+                            int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             const int32_t* wstart, void* o_lat, float* lse, float* part_o,
                             float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl);

@@ -17,10 +17,14 @@ struct ScheduleArgs {
     Schedule* sched;
     int32_t* wstart;        // [workers]
     int32_t* dev_status;
+    int align;              // sequences flattened in multiples of this many rows (1, or a tile for paged caches)
+    int64_t paged_cap;      // > 0: paged cache, a sequence is usable when 1 <= seq_len <= paged_cap (row_off unused)
 };
 
 // A sequence takes part with its length when 1 <= seq_len and its rows lie inside the
-// cache buffer; otherwise it counts as empty and MLA_DEV_BAD_LENGTH is raised.
+// cache buffer (paged: its length is covered by its block-table entries); otherwise it
+// counts as empty and MLA_DEV_BAD_LENGTH is raised.  With align > 1 every sequence spans
+// its length rounded up to a multiple of align in the flattened context.
 __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
     __shared__ long long warp_tot[32];
     __shared__ long long carry;
@@ -32,8 +36,10 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
         const int i = base + tid;
         long long x = 0;
         if (i < a.batch) {
-            const long long n = a.seq_len[i], o = a.row_off[i];
-            if (n >= 1 && o >= 0 && o + n <= a.cache_rows) x = n;
+            const long long n = a.seq_len[i];
+            const bool usable = a.paged_cap > 0 ? (n >= 1 && n <= a.paged_cap)
+                                                : (n >= 1 && a.row_off[i] >= 0 && a.row_off[i] + n <= a.cache_rows);
+            if (usable) x = (n + a.align - 1) / a.align * a.align;
             else atomicOr(a.dev_status, MLA_DEV_BAD_LENGTH);
             atomicMax(&longest, (unsigned long long)x);
         }
@@ -61,7 +67,8 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
         __syncthreads();
     }
     const long long total = carry;
-    const int64_t per = total > 0 ? (total + a.workers - 1) / a.workers : 1;
+    int64_t per = total > 0 ? (total + a.workers - 1) / a.workers : 1;
+    per = (per + a.align - 1) / a.align * a.align;          // range boundaries on whole tiles
     // Whole sequences per worker when there are no more sequences than workers and the
     // longest is within a quarter of the equal share: a little more time on the busiest
     // worker buys no cut sequence (no partial results, no merge, no mid-range reload of

@@ -25,7 +25,8 @@ class DecodeStep:
     def __init__(self, *, n_heads: int, d_h: int, d_c: int, d_r: int, hidden: int,
                  dtype: str, ctx_lens: Sequence[int], n_new: int, rope_base: float = 10000.0,
                  softmax_scale: float = 0.0, query_from_h: bool = False, d_q: Optional[int] = None,
-                 n_q: int = 1, num_splits: int = 0, extra_rows: int = 0, device: str = "cuda"):
+                 n_q: int = 1, num_splits: int = 0, extra_rows: int = 0, layout: str = "packed",
+                 block_size: int = 64, device: str = "cuda"):
         L.load()
         self.dims = L.make_dims(n_heads, d_h, d_c, d_r, hidden, rope_base, softmax_scale)
         self.dt = L.MLA_BF16 if dtype == "bf16" else L.MLA_F32
@@ -36,6 +37,8 @@ class DecodeStep:
         self.n_q = n_q
         if n_q > 1 and query_from_h:
             raise ValueError("several queries per sequence come with given q_C, q_R")
+        if n_q > 1 and layout != "packed":
+            raise ValueError("several queries per sequence run on the packed contiguous cache")
         Q = (n_q,) if n_q > 1 else ()
         self.ctx_lens = [int(x) for x in ctx_lens]
         self.query_from_h = query_from_h
@@ -56,7 +59,42 @@ class DecodeStep:
         self.pos0 = torch.tensor(self.ctx_lens, dtype=torch.int32, device=device)
         self.seq_len = torch.tensor([c + n_new for c in self.ctx_lens], dtype=torch.int32, device=device)
         self.max_seq_len = max(c + n_new for c in self.ctx_lens)
-        self.cache = torch.zeros(self.total_rows, self.row_elems, dtype=self.tdt, device=device)
+        # cache layout: "packed" rows [c ; k_R] in one contiguous buffer (the entry points
+        # without a layout), or through an mla_cache_layout: "split" (latents and rotary keys
+        # in two buffers), "paged" (blocks of block_size rows, scattered through a pool by a
+        # block table), "paged_split" (both)
+        self.layout = layout
+        self.paged = layout.startswith("paged")
+        self.split = layout.endswith("split")
+        if self.paged:
+            nblk = [(c + block_size - 1) // block_size for c in caps]
+            self.max_blocks = max(nblk)
+            pool = sum(nblk) + 1                            # one block never used
+            perm = torch.randperm(pool, generator=torch.Generator("cpu").manual_seed(12345))
+            table = torch.full((B, self.max_blocks), pool - 1, dtype=torch.int32)
+            k = 0
+            for b, n in enumerate(nblk):
+                table[b, :n] = perm[k:k + n].to(torch.int32)
+                k += n
+            self.block_table = table.to(device)
+            self.block_size = block_size
+            self.phys_rows = pool * block_size
+        else:
+            self.block_table = None
+            self.phys_rows = self.total_rows
+        if self.split:
+            self.kv = torch.zeros(self.phys_rows, d_c, dtype=self.tdt, device=device)
+            self.pe = torch.zeros(self.phys_rows, d_r, dtype=self.tdt, device=device)
+            self.cache = self.kv
+        else:
+            self.cache = torch.zeros(self.phys_rows, self.row_elems, dtype=self.tdt, device=device)
+            self.pe = None
+        self.cache_layout = None
+        if layout != "packed":
+            self.cache_layout = L.make_cache_layout(self.cache, self.pe, rows=self.phys_rows,
+                                                    block_table=self.block_table,
+                                                    block_size=block_size if self.paged else 0,
+                                                    max_blocks=self.max_blocks if self.paged else 0)
         # the step's inputs h, q_c, q_r are views of one contiguous buffer (each part starts
         # on a 256-byte boundary), so a caller can move them with one copy
         def _round(n):
@@ -103,10 +141,34 @@ class DecodeStep:
             self.out_workspace = torch.empty(max(self.out_ws_bytes, 256), dtype=torch.uint8, device=self.device)
             self.w_ov = None
 
+    def physical_rows(self, b: int, positions) -> torch.Tensor:
+        """Cache rows of the given positions of sequence b (the layout's addressing)."""
+        pos = torch.as_tensor(positions, dtype=torch.int64)
+        if not self.paged:
+            return pos + int(self.row_off[b].item())
+        table = self.block_table[b].to("cpu", torch.int64)
+        return table[pos // self.block_size] * self.block_size + pos % self.block_size
+
+    def read_rows(self, b: int, positions) -> torch.Tensor:
+        """Logical rows [c ; k_R] of sequence b at the given positions."""
+        idx = self.physical_rows(b, positions).to(self.device)
+        if self.split:
+            return torch.cat([self.kv[idx], self.pe[idx]], dim=1)
+        return self.cache[idx]
+
     def set_prefill(self, b: int, rows: torch.Tensor):
         n = rows.shape[0]
-        o = int(self.row_off[b].item())
-        self.cache[o:o + n].copy_(rows.to(self.tdt))
+        rows = rows.to(self.device, self.tdt)
+        if self.layout == "packed":
+            o = int(self.row_off[b].item())
+            self.cache[o:o + n].copy_(rows)
+            return
+        idx = self.physical_rows(b, range(n)).to(self.device)
+        if self.split:
+            self.kv[idx] = rows[:, :self.dims.d_c]
+            self.pe[idx] = rows[:, self.dims.d_c:]
+        else:
+            self.cache[idx] = rows
 
     def set_tokens(self, h: torch.Tensor):
         self.h.copy_(h)
@@ -119,6 +181,11 @@ class DecodeStep:
 
     # ------------------------------------------------------------------ path
     def append(self, stream=None):
+        if self.cache_layout is not None:
+            L.mla_cache_append_ex(self.dims, self.dt, self.batch, self.n_new, self.h, self.w["w_dkv"],
+                                  self.w["w_kr"], self.cache_layout, self.row_off, self.cap, self.pos0,
+                                  self.app_workspace, self.app_ws_bytes, self.dev_status, stream)
+            return
         L.mla_cache_append(self.dims, self.dt, self.batch, self.n_new, self.h, self.w["w_dkv"],
                            self.w["w_kr"], self.row_off, self.cap, self.pos0, self.cache,
                            self.total_rows, self.app_workspace, self.app_ws_bytes, self.dev_status,
@@ -148,6 +215,12 @@ class DecodeStep:
         if ns != self.num_splits:
             nb = L.mla_decode_workspace_size(self.dims, self.dt, self.batch, self.max_seq_len, ns)
             ws = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        if self.cache_layout is not None:
+            L.mla_decode_absorbed_ex(self.dims, self.dt, self.batch, self.q_c, self.q_r, self.w["w_uk"],
+                                     self.cache_layout, self.row_off, self.seq_len, self.max_seq_len, ns, ws,
+                                     ws.numel(), self.o_lat if o_lat is None else o_lat,
+                                     self.lse if lse is None else lse, self.dev_status, stream)
+            return
         L.mla_decode_absorbed(self.dims, self.dt, self.batch, self.q_c, self.q_r, self.w["w_uk"],
                               self.cache, self.total_rows, self.row_off, self.seq_len,
                               self.max_seq_len, ns, ws,
@@ -195,7 +268,7 @@ class DecodeStep:
         reads no cache row), so the append runs on a second stream beside it; the attention
         waits for both.  Under stream capture this becomes two branches of the graph.
         """
-        if self.n_q > 1:                        # the multi-query decode is one call
+        if self.n_q > 1 or self.cache_layout is not None:   # the decode is one call
             self.step_serial(stream)
             return
         main = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(self.device)
@@ -235,11 +308,11 @@ class DecodeStep:
         return g
 
     def new_rows(self, b: int) -> torch.Tensor:
-        o = int(self.row_off[b].item()) + self.ctx_lens[b]
-        return self.cache[o:o + self.n_new]
+        return self.read_rows(b, range(self.ctx_lens[b], self.ctx_lens[b] + self.n_new))
 
 
-def from_workload(wl, ctx_lens=None, num_splits: int = 0, device: str = "cuda", load_inputs: bool = True):
+def from_workload(wl, ctx_lens=None, num_splits: int = 0, device: str = "cuda", load_inputs: bool = True,
+                  layout: str = "packed", block_size: int = 64):
     """A ``DecodeStep`` for a synthetic workload, inputs uploaded from the seeded generators."""
     import mla_inputs
     if ctx_lens is None:
@@ -247,7 +320,7 @@ def from_workload(wl, ctx_lens=None, num_splits: int = 0, device: str = "cuda", 
     st = DecodeStep(n_heads=wl.n_heads, d_h=wl.d_h, d_c=wl.d_c, d_r=wl.d_r, hidden=wl.hidden,
                     dtype=wl.dtype, ctx_lens=ctx_lens, n_new=wl.n_new, rope_base=wl.rope_base,
                     query_from_h=wl.query_from_h, d_q=wl.d_q, n_q=wl.n_q, num_splits=num_splits,
-                    device=device)
+                    layout=layout, block_size=block_size, device=device)
     if load_inputs:
         weights, h, queries = mla_inputs.make_all(wl)
         st.set_weights(weights)

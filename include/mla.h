@@ -83,6 +83,30 @@ typedef struct {
 } mla_dims;
 
 /*
+ * Where the latent cache lives, for mla_cache_append_ex and mla_decode_absorbed_ex (the
+ * other calls take one packed contiguous buffer).  Two choices, freely combined:
+ * - packed rows [c ; k_R] in kv (pe NULL), or the latents in kv and the rotary keys in a
+ *   buffer of their own, pe, row for row ("DeepSeek MLA: 4 Attention Methods Compared",
+ *   section "Why DeepSeek reconstruction does not erase the MLA benefit": separate
+ *   kv_cache and pe_cache);
+ * - contiguous sequences (block_table NULL: position t of sequence b is row row_off[b] + t)
+ *   or a paged cache ("The Journey to Multi-Head Latent Attention", section "Why the KV
+ *   cache explodes": paged attention): position t of sequence b is row
+ *   block_table[b * max_blocks + t / block_size] * block_size + t % block_size.
+ * Rows are bf16, 16-byte aligned, in DeepSeek's shape (d_c = 512, d_r = 64).
+ */
+typedef struct {
+    void* kv;                   /* latent rows (d_c elements each), or packed rows when pe is NULL */
+    void* pe;                   /* rotary-key rows (d_r elements each), or NULL */
+    int64_t kv_stride;          /* elements from one kv row to the next: >= d_c (>= d_c + d_r packed), multiple of 8 */
+    int64_t pe_stride;          /* elements from one pe row to the next: >= d_r, multiple of 8 */
+    int64_t rows;               /* rows in kv (and in pe), at least 32 */
+    const int32_t* block_table; /* device [batch, max_blocks] physical block of each logical block, or NULL */
+    int32_t block_size;         /* rows per block, a positive multiple of 64 (paged only) */
+    int32_t max_blocks;         /* block-table entries per sequence (paged only) */
+} mla_cache_layout;
+
+/*
  * mla_cache_append -- write the latent rows of new tokens into the cache.
  * Defines c = W_DKV h and k_R = RoPE(W_KR h, pos) ("Grouped-query and latent
  * attention", sections "Multi-head latent attention" and "Why a separate rotary
@@ -110,6 +134,21 @@ MLA_API mla_status mla_cache_append(const mla_dims* dims, mla_dtype dtype, int32
                             const int64_t* row_off, const int32_t* cap, const int32_t* pos0,
                             void* cache, int64_t cache_rows, void* workspace,
                             size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * mla_cache_append_ex -- mla_cache_append into a cache described by `cache` (see
+ * mla_cache_layout).  row_off is read only for a contiguous layout (may be NULL when
+ * paged); cap[b] bounds the positions of sequence b as before, and a paged sequence also
+ * needs cap[b] <= max_blocks * block_size and every written row inside the buffer
+ * (MLA_DEV_BAD_POSITION otherwise, that row skipped).  Runs on tensor cores only: bf16,
+ * d_c = 512, d_r = 64, d_h and hidden multiples of 128 and 64; MLA_ERR_UNSUPPORTED
+ * otherwise.  Same workspace as mla_cache_append.
+ */
+MLA_API mla_status mla_cache_append_ex(const mla_dims* dims, mla_dtype dtype, int32_t batch, int32_t n_new,
+                               const void* h, const void* w_dkv, const void* w_kr,
+                               const mla_cache_layout* cache, const int64_t* row_off, const int32_t* cap,
+                               const int32_t* pos0, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, void* stream);
 
 /*
  * mla_append_workspace_size -- bytes of device workspace mla_cache_append needs (bf16
@@ -202,6 +241,21 @@ MLA_API mla_status mla_decode_absorbed(const mla_dims* dims, mla_dtype dtype, in
                                const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
                                void* workspace, size_t workspace_bytes,
                                void* o_lat, float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * mla_decode_absorbed_ex -- mla_decode_absorbed over a cache described by `cache` (see
+ * mla_cache_layout); row_off is read only for a contiguous layout.  A paged sequence is
+ * usable when 1 <= seq_len[b] <= max_blocks * block_size (MLA_DEV_BAD_LENGTH otherwise);
+ * block-table entries are not checked: a block outside the buffer reads as zeros.  Runs
+ * on the tensor-core kernel only (bf16, d_c = 512, d_r = 64, n_heads <= 128);
+ * MLA_ERR_UNSUPPORTED otherwise.  Same workspace as mla_decode_absorbed.
+ */
+MLA_API mla_status mla_decode_absorbed_ex(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                  const void* q_c, const void* q_r, const void* w_uk,
+                                  const mla_cache_layout* cache, const int64_t* row_off,
+                                  const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                                  void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                  int32_t* dev_status, void* stream);
 
 /*
  * mla_decode_absorbed_multi -- n_q causal queries per sequence (several new tokens decoded

@@ -100,3 +100,23 @@ def test_workspace_size_explicit_splits():
     b = mla.mla_decode_workspace_size(d, mla.MLA_F32, 1, 129, 7)
     assert 0 < a < b and a % 256 == 0 and b % 256 == 0
     assert mla.mla_decode_workspace_size(d, mla.MLA_F32, 0, 129, 1) == 0
+
+
+def test_cache_layout_checks_on_host():
+    """Layouts are checked before anything is enqueued: unsupported shapes, misaligned or
+    too-short strides, block sizes that are not whole tiles."""
+    lib = mla.load()
+    fake = 1 << 12                              # 16-byte aligned, never dereferenced
+    v3 = mla.make_dims(128, 128, 512, 64, 7168)
+    good = mla.MlaCacheLayout(fake, fake, 512, 64, 1 << 16, None, 0, 0)
+    bad_stride = mla.MlaCacheLayout(fake, fake, 500, 64, 1 << 16, None, 0, 0)
+    bad_block = mla.MlaCacheLayout(fake, None, 576, 0, 1 << 16, fake, 96, 8)
+    args = lambda lay: (ctypes.byref(v3), mla.MLA_BF16, 4, fake, fake, fake, ctypes.byref(lay), fake, fake, 4096,
+                        0, fake, 1 << 30, fake, None, fake, None)
+    assert lib.mla_decode_absorbed_ex(*args(bad_stride)) == mla.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_absorbed_ex(*args(bad_block)) == mla.MLA_ERR_INVALID_ARG
+    small = mla.make_dims(4, 16, 32, 8, 64)
+    assert lib.mla_decode_absorbed_ex(ctypes.byref(small), mla.MLA_BF16, 4, fake, fake, fake, ctypes.byref(good),
+                                      fake, fake, 16, 0, fake, 1 << 30, fake, None, fake, None) == mla.MLA_ERR_UNSUPPORTED
+    assert lib.mla_cache_append_ex(ctypes.byref(small), mla.MLA_BF16, 1, 1, fake, fake, fake, ctypes.byref(good),
+                                   fake, fake, fake, fake, 1 << 20, fake, None) == mla.MLA_ERR_UNSUPPORTED

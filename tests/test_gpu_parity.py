@@ -233,6 +233,45 @@ def test_output_projection_two_step_and_merged(name, seqs):
         assert_parity(u_m[b], u_ref, wl.dtype, f"seq {b} u (merged)")
 
 
+LAYOUTS = [("split", 64), ("paged", 64), ("paged", 128), ("paged_split", 256)]
+
+
+@pytest.mark.parametrize("layout,block_size", LAYOUTS)
+@pytest.mark.parametrize("lens,num_splits", [(None, 0), ([1, 30, 63, 64, 65, 127, 200, 1000], 3),
+                                             ([1, 30, 63, 64, 65, 127, 200, 1000], 0)])
+def test_cache_layouts(layout, block_size, lens, num_splits):
+    """The cache append and the decode through an mla_cache_layout: latents and rotary keys
+    in separate buffers and/or a paged pool whose blocks a seeded shuffle scatters; ranges
+    cut sequences (a paged cache flattens them in whole 64-row tiles)."""
+    wl = mla_inputs.WORKLOADS["small_bf16"]
+    if lens is not None:
+        wl = dataclasses.replace(wl, name="small_bf16_layout_tails", batch=len(lens), n_new=1)
+    st = runner.from_workload(wl, ctx_lens=lens, num_splits=num_splits, layout=layout, block_size=block_size)
+    st.step()
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) == 0
+    for b in range(wl.batch):
+        _compare(st, wl, b, what=f" {layout}/{block_size} splits={num_splits}")
+    if layout == "split":
+        # the same schedule as the packed cache: the same bits
+        ref = runner.from_workload(wl, ctx_lens=lens, num_splits=num_splits)
+        ref.step()
+        torch.cuda.synchronize()
+        assert torch.equal(ref.o_lat, st.o_lat) and torch.equal(ref.out, st.out)
+
+
+@pytest.mark.parametrize("layout", ["paged", "paged_split"])
+def test_v3_b64_paged_sampled(layout):
+    """The bench's V3 batch-64 decode with a paged cache of 64-row blocks."""
+    wl = mla_inputs.WORKLOADS["v3_b64_l4096"]
+    st = runner.from_workload(wl, layout=layout, block_size=64)
+    st.step()
+    torch.cuda.synchronize()
+    assert int(st.dev_status.item()) == 0
+    for b in (0, 40):
+        _compare(st, wl, b, heads=SAMPLED_HEADS, what=f" {layout}")
+
+
 def test_cuda_core_bf16_odd_shapes():
     """bf16 shapes outside the tensor-core kernels (latent 256, rotary 32, 8 heads of
     width 64): the append, fold, attention and W_UV all run on CUDA cores."""
