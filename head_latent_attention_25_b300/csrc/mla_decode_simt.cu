@@ -141,11 +141,15 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
 }
 
 // ------------------------------------------------------------------ merge
-// Grid (batch, head groups of 8): warp w of a block merges head 8*blockIdx.y + w of a
-// sequence that was cut across workers.  Lane j keeps the log2-sum-exps of pieces
-// j, j+32, ... in registers (one load round), the warp reduces their maximum and sum
-// with shuffles, and each piece's weight is broadcast from its lane while every lane
-// adds its 16 columns of that piece (4 float4 loads, a warp reads 2 KB contiguously).
+// Grid (batch, head groups of 8, column chunks): warp w of a block merges head
+// 8*blockIdx.y + w of a sequence that was cut across workers.  Lane j keeps the
+// log2-sum-exps of pieces j, j+32, ... in registers (one load round), the warp reduces
+// their maximum and sum with shuffles, and each piece's weight is broadcast from its
+// lane while every lane adds its kCols columns of that piece (float4 loads, 64 / kCols
+// pieces in flight).  Large batches take 16 columns a lane and one chunk (a warp reads
+// 2 KB of a piece contiguously); small batches, whose few sequences are cut into many
+// pieces, take 4 columns a lane and spread the column rounds over blockIdx.z, so that
+// enough blocks stream the partial results.
 constexpr int kMergeHeads = 8;
 constexpr int kMergeRegs = 4;                   // pieces held per lane before the slow path
 
@@ -154,7 +158,7 @@ __device__ __forceinline__ int64_t piece_slot(int64_t w, int64_t seq_begin, int6
     return 2 * w + (seq_begin <= w * per ? 0 : 1);
 }
 
-template <typename Tout>
+template <typename Tout, int kCols>
 __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* __restrict__ cum,
                                                                  const Schedule* __restrict__ sched,
                                                                  const float* __restrict__ part_o,
@@ -170,6 +174,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
     const int64_t per = sched->per;
     Tout* out = o_lat + ((int64_t)b * n_h + h) * d_c;
     if (seq1 == seq0) {                         // empty or rejected by the schedule
+        if (blockIdx.z != 0) return;
         for (int c = 2 * lane; c < d_c; c += 64) st2(out + c, 0.f, 0.f);
         if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = -INFINITY;
         return;
@@ -197,12 +202,12 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
         L += exp2f(part_l[piece_slot(first_w + p, seq0, per) * n_h + h] - mx);
     L = warp_sum(L);
     const float inv = 1.f / L;
-    if (lane == 0 && lse) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
-    // pass 2: lane owns columns [16 lane, 16 lane + 16) (+ 512 k for wider latents)
-    constexpr int kCols = 16;
+    if (lane == 0 && lse && blockIdx.z == 0) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
+    // pass 2: in round rd a lane owns columns [kCols lane, kCols lane + kCols) + 32 kCols rd
+    constexpr int kIn = 64 / kCols;             // pieces in flight (16 float4 loads a lane)
     const bool vec = (d_c % kCols) == 0;        // float4 loads stay aligned
     const int rounds = (d_c + 32 * kCols - 1) / (32 * kCols);
-    for (int rd = 0; rd < rounds; ++rd) {
+    for (int rd = blockIdx.z; rd < rounds; rd += gridDim.z) {
         // every lane runs the loop the same number of times (the shuffles need all 32)
         const int c0 = kCols * lane + 32 * kCols * rd;
         float acc[kCols];
@@ -227,26 +232,28 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
                     if (e < nc) acc[e] = fmaf(wp, src[e], acc[e]);
             }
         };
-        if (vec && nc == kCols) {
-            // four pieces per round: sixteen 16-byte loads of a lane in flight together
+        if (vec) {
+            // kIn pieces per round: sixteen 16-byte loads of a lane in flight together.  The
+            // branch is warp-uniform (the shuffles need all 32 lanes); with vec a lane's
+            // chunk is either whole (nc == kCols) or past the end (nc == 0, no loads).
 #pragma unroll
             for (int k = 0; k < kMergeRegs; ++k) {
                 if (32 * k >= np) break;
                 const int nj = (int)min((int64_t)32, np - 32 * k);
-                for (int j0 = 0; j0 < nj; j0 += 4) {
-                    float4 v[4][kCols / 4];
-                    float wp[4];
+                for (int j0 = 0; j0 < nj; j0 += kIn) {
+                    float4 v[kIn][kCols / 4];
+                    float wp[kIn];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < kIn; ++u) {
                         const int j = j0 + u < nj ? j0 + u : j0;
                         wp[u] = j0 + u < nj ? exp2f(__shfl_sync(0xffffffffu, lr[k], j) - mx) * inv : 0.f;
                         const float4* src = reinterpret_cast<const float4*>(
                             part_o + (piece_slot(first_w + 32 * k + j, seq0, per) * n_h + h) * d_c + c0);
 #pragma unroll
-                        for (int q = 0; q < kCols / 4; ++q) v[u][q] = src[q];
+                        for (int q = 0; q < kCols / 4; ++q) v[u][q] = nc ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < kIn; ++u)
 #pragma unroll
                         for (int q = 0; q < kCols / 4; ++q) {
                             acc[4 * q] = fmaf(wp[u], v[u][q].x, acc[4 * q]);
@@ -330,14 +337,23 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,
                          const void* sched, const float* part_o, const float* part_l, void* o_lat,
                          float* lse, cudaStream_t s, bool pdl) {
-    const dim3 grid(batch, (d.n_heads + kMergeHeads - 1) / kMergeHeads);
+    const int groups = (d.n_heads + kMergeHeads - 1) / kMergeHeads;
+    // fewer (sequence, head group) blocks than two per SM: narrow column chunks over blockIdx.z
+    const bool narrow = (int64_t)batch * groups < 2 * 148;
+    const int chunks = narrow ? (d.d_c + 127) / 128 : 1;
+    const dim3 grid(batch, groups, chunks);
+    const dim3 block(32 * kMergeHeads);
     cudaError_t e;
     if (bf16)
-        e = launch_ex(merge_kernel<__nv_bfloat16>, grid, dim3(32 * kMergeHeads), 0, s, pdl, cum,
-                      (const Schedule*)sched, part_o, part_l, (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
+        e = narrow ? launch_ex(merge_kernel<__nv_bfloat16, 4>, grid, block, 0, s, pdl, cum, (const Schedule*)sched,
+                               part_o, part_l, (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c)
+                   : launch_ex(merge_kernel<__nv_bfloat16, 16>, grid, block, 0, s, pdl, cum, (const Schedule*)sched,
+                               part_o, part_l, (__nv_bfloat16*)o_lat, lse, d.n_heads, d.d_c);
     else
-        e = launch_ex(merge_kernel<float>, grid, dim3(32 * kMergeHeads), 0, s, pdl, cum, (const Schedule*)sched,
-                      part_o, part_l, (float*)o_lat, lse, d.n_heads, d.d_c);
+        e = narrow ? launch_ex(merge_kernel<float, 4>, grid, block, 0, s, pdl, cum, (const Schedule*)sched,
+                               part_o, part_l, (float*)o_lat, lse, d.n_heads, d.d_c)
+                   : launch_ex(merge_kernel<float, 16>, grid, block, 0, s, pdl, cum, (const Schedule*)sched,
+                               part_o, part_l, (float*)o_lat, lse, d.n_heads, d.d_c);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
 }

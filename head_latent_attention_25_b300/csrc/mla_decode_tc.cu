@@ -250,7 +250,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
-        mbar_init(bar(B_QFULL), 128);
+        // Q' of a piece is in place: the first piece's is loaded by the softmax groups (latent
+        // part) and the epilogue warps (rotary part), later ones by the epilogue warps alone,
+        // which then arrive three times each
+        mbar_init(bar(B_QFULL), 384);
         mbar_init(bar(B_QEMPTY), 2);                  // one commit per score issuer
         // score and value barriers per tile parity: each phase of one is waited for in
         // order by the issuer or group that owns (or follows) those tiles
@@ -441,6 +444,34 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const uint32_t peer_x = mapa(sX + xb * kXBytes, peer);
             const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
                 float* mshare = (float*)(sm + kOffMh);
+            {
+                // the first piece's Q' (latent part) into tensor memory: group grp loads the
+                // 64-column chunks 2 grp and 2 grp + 1 of this CTA's half, one round of loads,
+                // while the epilogue warps load the rotary part (at the start of a launch the
+                // three warpgroups together cut the wait for Q')
+                SegWalk<kTiled> w0;
+                w0.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                Seg s0;
+                if (w0.next(s0)) {
+                    const bool row_ok = i < a.n_h;
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        a.qp + ((int64_t)s0.b * a.n_h + (row_ok ? i : 0)) * kRowElems) + rank * 32 + 16 * grp;
+                    const uint4 zero = make_uint4(0, 0, 0, 0);
+                    uint32_t r0[32], r1[32];
+    #pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = row_ok ? src[c] : zero;
+                        const uint4 w = row_ok ? src[8 + c] : zero;
+                        r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
+                        r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
+                    }
+                    tmem_st32u(tmem + lane_base + kColQ + 64 * grp, r0);
+                    tmem_st32u(tmem + lane_base + kColQ + 64 * grp + 32, r1);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(B_QFULL));
+                }
+            }
             TileIt<kTiled> co;
             co.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
             bool ok = true;
@@ -600,7 +631,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             bool have = walk.next(cur);
             uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
             // Q' of one piece into TMEM columns kColQ.. (zero rows for heads >= n_h)
-            auto load_q = [&](const Seg& sg) {
+            // first: the softmax groups load this piece's latent part (the first piece)
+            auto load_q = [&](const Seg& sg, bool first) {
                 const bool row_ok = i < a.n_h;
                 const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
                 const uint4 zero = make_uint4(0, 0, 0, 0);
@@ -612,6 +644,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     for (int c = 0; c < 4; ++c)
                         *(uint4*)(qrow + ((c ^ ((i >> 1) & 3)) << 4)) = row_ok ? src[64 + rank * 4 + c] : zero;
                     fence_proxy_async_smem();
+                }
+                if (first) {
+                    tc_fence_before();
+                    mbar_arrive(bar(B_QFULL));
+                    return;
                 }
                 // latent columns [256r, 256r + 256) into tensor memory, two chunks of 64 bf16
                 // (32 TMEM columns each) per round of loads
@@ -630,10 +667,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(B_QFULL));
+                mbar_arrive_cnt(bar(B_QFULL), 3);
             };
             bool ok = true;
-            if (have) load_q(cur);
+            if (have) load_q(cur, true);
             while (ok && have) {
                 t_end += (uint32_t)tiles_of(cur);
                 const bool more = walk.next(nxt);
@@ -641,7 +678,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     // the score MMAs of this piece are done with Q'
                     if (!(ok = wwait<false>(bar(B_QEMPTY), si & 1, ctl))) break;
                     tc_fence_after();
-                    load_q(nxt);
+                    load_q(nxt, false);
                 }
                 // epilogue of this piece: O_r / l, log2-sum-exp
                 if (!(ok = wwait<false>(bar(B_STATS + (si & 3)), (si >> 2) & 1, ctl))) break;
