@@ -4,7 +4,7 @@ The computation lives in the CUDA library ``libmla.so`` (C ABI in
 ``include/mla.h``); this package only loads it and marshals arguments.
 """
 from ._lib import (  # noqa: F401
-    EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT,
+    EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT, MLA_DEV_SMEM_ALIGN,
     MLA_ERR_CUDA, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_F32, MLA_OK,
     MlaCacheLayout, MlaDims, MlaError, load, make_cache_layout, make_dims, mla_append_workspace_size,
     mla_cache_append, mla_cache_append_ex, mla_decode_absorbed, mla_decode_absorbed_ex,

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA = range(5)
 MLA_F32, MLA_BF16 = 0, 1
-MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT = 0x1, 0x2, 0x4
+MLA_DEV_BAD_LENGTH, MLA_DEV_BAD_POSITION, MLA_DEV_TIMEOUT, MLA_DEV_SMEM_ALIGN = 0x1, 0x2, 0x4, 0x8
 
 EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size",
             "mla_decode_absorbed", "mla_project_out", "mla_status_string", "mla_launch_count",

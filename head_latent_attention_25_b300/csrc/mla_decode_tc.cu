@@ -63,20 +63,26 @@ constexpr uint32_t kXResBytes = kHeads * kTok * 2;
 constexpr uint32_t kXBytes = kXResBytes + kHeads * 4;
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffP = kOffX + 2 * kXBytes;          // P: 128 heads x 64 rows bf16, K-major, 128B swizzle
-constexpr uint32_t kOffQR = kOffP + kHeads * 128;         // rotary part of Q'_r: 128 x 32 bf16, 64B swizzle
+// latent chunks 2 and 3 (columns 128..255 of this CTA's half) of Q'_r: the A operand of
+// half of the latent score MMAs, 2 x (128 heads x 64 bf16), K-major, 128B swizzle
+constexpr uint32_t kOffQL = kOffX + 2 * kXBytes;
+constexpr uint32_t kQLChunk = kHeads * 128;
+constexpr uint32_t kOffQR = kOffQL + 2 * kQLChunk;       // rotary part of Q'_r: 128 x 32 bf16, 64B swizzle
 constexpr uint32_t kOffStats = kOffQR + kHeads * 64;      // [piece % 4][group][m, l][head] fp32
 constexpr uint32_t kOffMh = kOffStats + 4 * 2 * 2 * kHeads * 4;   // [tile parity][head] running max
 constexpr uint32_t kOffBar = kOffMh + 2 * kHeads * 4;
 constexpr uint32_t kBarBytes = 320;                      // mbarriers, then the TMEM slot and abort flag
-constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;   // + alignment slack
+// No alignment slack: dynamic shared memory starts on a 1024-byte boundary (it follows the
+// 1 KB reserved at the bottom of a CTA's window, and the kernel has no static shared
+// memory); the kernel checks this and returns MLA_DEV_SMEM_ALIGN otherwise.
+constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffP % 1024 == 0 && kOffQR % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(kOffQL % 1024 == 0 && kQLChunk % 1024 == 0, "swizzled operands need 1024-byte alignment");
 
 // barrier indices
 enum : int {
     B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
-    B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_VDONE, B_OFREE = B_VDONE + 2, B_XFULL,
+    B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_VDONE = B_PFULL + 2, B_OFREE = B_VDONE + 2, B_XFULL,
     B_XEMPTY = B_XFULL + 2, B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS,
     B_COUNT = B_XCONS + 2
 };
@@ -87,7 +93,9 @@ constexpr uint32_t kOffAbort = kOffTslot + 4;
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;          // O_r: 256 fp32 columns
-constexpr uint32_t kColQ = 256;        // latent part of Q'_r: 256 bf16 = 128 columns
+constexpr uint32_t kColQ = 256;        // latent chunks 0, 1 of Q'_r: 128 bf16 = 64 columns
+constexpr uint32_t kColP = 320;        // P[2] (by tile parity): 128 heads x 64 rows bf16 = 2 x 32 columns,
+                                       // the A operand of the value MMA
 constexpr uint32_t kColS = 384;        // S[2] (by tile parity): 2 x 64 fp32 columns
 
 struct TcArgs {
@@ -218,6 +226,21 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 }
 
 __device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return smem_desc(a, 16, 1024, kSwizzle128B); }
+
+// Row i of Q'_r's latent chunks 2 and 3 into shared memory: two 128-head x 64-column bf16
+// chunks, K-major with the 128B swizzle (16-byte unit c of row i stored at unit c ^ (i & 7)).
+// src: the row's 16 uint4 (chunk 2 then chunk 3), or null for a zero row.
+__device__ __forceinline__ void store_ql_row(uint8_t* ql, int i, const uint4* src) {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = src ? src[8 * h + c] : zero;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) *(uint4*)(ql + h * kQLChunk + i * 128 + ((c ^ (i & 7)) << 4)) = v[c];
+    }
+}
 __device__ __forceinline__ uint64_t kdesc64(uint32_t a) { return smem_desc(a, 16, 512, kSwizzle64B); }
 // MN-major 128B-swizzled B: 64-column atoms one TMA box (kTBox bytes) apart, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t mndesc128(uint32_t a) { return smem_desc(a, kTBox, 1024, kSwizzle128B); }
@@ -234,8 +257,12 @@ template <bool kTiled>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
                 TcArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw;
+    if (smem_addr(sm) & 1023u) {        // the same in every CTA of the launch: all return here
+        if (threadIdx.x == 0) atomicOr(a.dev_status, MLA_DEV_SMEM_ALIGN);
+        return;
+    }
     const uint32_t base = smem_addr(sm);
     const uint32_t sStage = base + kOffStage, sX = base + kOffX;
     uint64_t* bars = (uint64_t*)(sm + kOffBar);
@@ -261,8 +288,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_SEMPTY + i), 128);
             mbar_init(bar(B_VDONE + i), 1);
+            mbar_init(bar(B_PFULL + i), 128);       // the group that owns the tile parity
         }
-        mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_OFREE), 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_XFULL + i), 1);
@@ -376,7 +403,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             if (lane == 0) {
                 const uint32_t par = warp == 1 ? 0u : 1u;
                 const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
-                const uint32_t sQR = base + kOffQR;
+                const uint32_t sQL = base + kOffQL, sQR = base + kOffQR;
                 TileIt<kTiled> it;
                 it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 bool ok = true;
@@ -390,9 +417,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         tc_fence_after();
                         const uint32_t stage = sStage + st * kStageBytes;
                         const uint32_t d = tmem + kColS + 64 * par;
-                        for (int kk = 0; kk < 16; ++kk)
+                        // latent chunks 0, 1: A (Q') from tensor memory; chunks 2, 3 and the
+                        // rotary part: A from shared memory
+                        for (int kk = 0; kk < 8; ++kk)
                             mma_bf16_ts(d, tmem + kColQ + 8 * kk, kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)),
                                         id_s, kk ? 1u : 0u);
+                        for (int kk = 8; kk < 16; ++kk)
+                            mma_bf16(d, kdesc128(sQL + ((kk >> 2) - 2) * kQLChunk + 32 * (kk & 3)),
+                                     kdesc128(stage + (kk >> 2) * kTBox + 32 * (kk & 3)), id_s, 1u);
                         for (int kk = 0; kk < 2; ++kk)
                             mma_bf16(d, kdesc64(sQR + 32 * kk), kdesc64(stage + 4 * kTBox + 32 * kk), id_s, 1u);
                         mma_commit(bar(B_SFULL + par));
@@ -404,23 +436,22 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             }
         } else if (warp == 2) {
             // ------------------------------------------------------------ value MMA issuer
-            // O_r += P C_r: P (bf16, 128 heads x 64 rows) from shared memory, the tile's
+            // O_r += P C_r: P (bf16, 128 heads x 64 rows) from tensor memory, the tile's
             // latent half as an MN-major B operand.  A stage is released here: the value MMA
             // of a tile always completes after its score MMA (the softmax in between needs it).
             if (lane == 0) {
                 const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
-                const uint32_t sP = base + kOffP;
                 TileIt<kTiled> it;
                 it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 bool ok = true;
                 while (ok && it.next()) {
                     const uint32_t T = it.T, st = T % kStages;
-                    if (!(ok = wait<false>(bar(B_PFULL), T & 1, ctl))) break;
+                    if (!(ok = wait<false>(bar(B_PFULL + (T & 1)), (T >> 1) & 1, ctl))) break;
                     if (it.first_tile() && it.si > 0 && !(ok = wait<false>(bar(B_OFREE), (it.si - 1) & 1, ctl))) break;
                     tc_fence_after();
                     const uint32_t stage = sStage + st * kStageBytes;
                     for (int k = 0; k < kTok / 16; ++k)
-                        mma_bf16(tmem + kColO, kdesc128(sP + 32 * k), mndesc128(stage + 2048 * k), id_o,
+                        mma_bf16_ts(tmem + kColO, tmem + kColP + 32 * (T & 1) + 8 * k, mndesc128(stage + 2048 * k), id_o,
                                  (it.first_tile() && k == 0) ? 0u : 1u);
                     mma_commit(bar(B_EMPTY + st));
                     mma_commit(bar(B_VDONE + (T & 1)));
@@ -445,10 +476,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             const uint32_t peer_xfull = mapa(bar(B_XFULL + xb), peer);
                 float* mshare = (float*)(sm + kOffMh);
             {
-                // the first piece's Q' (latent part) into tensor memory: group grp loads the
-                // 64-column chunks 2 grp and 2 grp + 1 of this CTA's half, one round of loads,
-                // while the epilogue warps load the rotary part (at the start of a launch the
-                // three warpgroups together cut the wait for Q')
+                // the first piece's Q' (latent part): group grp loads the 64-column chunks
+                // 2 grp and 2 grp + 1 of this CTA's half (group 0 into tensor memory, group 1
+                // into shared memory), one round of loads, while the epilogue warps load the
+                // rotary part (at the start of a launch the three warpgroups together cut the
+                // wait for Q')
                 SegWalk<kTiled> w0;
                 w0.init(a.cum, a.seq_len, a.wstart[g], g, S);
                 Seg s0;
@@ -456,18 +488,23 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     const bool row_ok = i < a.n_h;
                     const uint4* src = reinterpret_cast<const uint4*>(
                         a.qp + ((int64_t)s0.b * a.n_h + (row_ok ? i : 0)) * kRowElems) + rank * 32 + 16 * grp;
-                    const uint4 zero = make_uint4(0, 0, 0, 0);
-                    uint32_t r0[32], r1[32];
+                    if (grp == 0) {                 // chunks 0, 1: tensor memory
+                        const uint4 zero = make_uint4(0, 0, 0, 0);
+                        uint32_t r0[32], r1[32];
     #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = row_ok ? src[c] : zero;
-                        const uint4 w = row_ok ? src[8 + c] : zero;
-                        r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
-                        r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 v = row_ok ? src[c] : zero;
+                            const uint4 w = row_ok ? src[8 + c] : zero;
+                            r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
+                            r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
+                        }
+                        tmem_st32u(tmem + lane_base + kColQ, r0);
+                        tmem_st32u(tmem + lane_base + kColQ + 32, r1);
+                        tmem_wait_st();
+                    } else {                        // chunks 2, 3: shared memory
+                        store_ql_row(sm + kOffQL, i, row_ok ? src : nullptr);
+                        fence_proxy_async_smem();
                     }
-                    tmem_st32u(tmem + lane_base + kColQ + 64 * grp, r0);
-                    tmem_st32u(tmem + lane_base + kColQ + 64 * grp + 32, r1);
-                    tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(bar(B_QFULL));
                 }
@@ -575,12 +612,16 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         packed[j] = *reinterpret_cast<const uint32_t*>(&h2);
                     }
                     l_g += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    // the value MMA of the previous tile has finished with P and O
-                    if (T > 0) {
-                        if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                    // P[T % 2] is free once the value MMA of tile T - 2 has finished
+                    if (T >= 2) {
+                        if (!(ok = wwait<false>(bar(B_VDONE + (T & 1)), ((T - 2) >> 1) & 1, ctl))) break;
                         tc_fence_after();
                     }
                     if (!co.first_tile() && __any_sync(0xffffffffu, need)) {
+                        // a moved maximum rescales O: after the value MMA of tile T - 1 (whose P
+                        // is on the old scale), before that of tile T (held back by PFULL)
+                        if (!(ok = wwait<false>(bar(B_VDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl))) break;
+                        tc_fence_after();
                         for (int c = 0; c < kLatHalf / 16; ++c) {
                             float o[16];
                             tmem_ld16(tmem + lane_base + kColO + 16 * c, o);
@@ -591,13 +632,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                             tmem_st16(tmem + lane_base + kColO + 16 * c, u);
                         }
                     }
-                    {   // row i of P: 128 bytes, 16-byte chunk c stored at chunk c ^ (i & 7) (128B swizzle)
-                        uint8_t* prow = sm + kOffP + i * 128;
-    #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *(uint4*)(prow + ((c ^ (i & 7)) << 4)) =
-                                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                    }
+                    // row i of P into tensor memory (lane i, two bf16 per column, the lower row
+                    // in the low half: the A operand layout of the value MMA)
+                    tmem_st32u(tmem + lane_base + kColP + 32 * xb, packed);
                     if (valid < kTok) {
                         // the value MMA must not see rows of the tile beyond the piece (they may
                         // hold anything): zero them in this CTA's latent half of the stage
@@ -606,11 +643,11 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                             const int r = valid + e / 32, box = (e / 8) & 3, ch = e & 7;
                             *(uint4*)(stage + box * kTBox + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
                         }
+                        fence_proxy_async_smem();               // the zeroed rows to the tensor core
                     }
-                    fence_proxy_async_smem();                   // P (and zeroed rows) to the tensor core
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(bar(B_PFULL));
+                    mbar_arrive(bar(B_PFULL + xb));
                 }
                 if (co.last_tile()) {
                     // this group's share of the piece's statistics
@@ -630,15 +667,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             Seg cur, nxt;
             bool have = walk.next(cur);
             uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
-            // Q' of one piece into TMEM columns kColQ.. (zero rows for heads >= n_h)
-            // first: the softmax groups load this piece's latent part (the first piece)
+            // Q' of one piece (zero rows for heads >= n_h): latent chunks 0, 1 into tensor
+            // memory, latent chunks 2, 3 and the rotary part into shared memory.  first: the
+            // softmax groups load the latent part (the first piece of a launch), this
+            // warpgroup only the rotary part.
             auto load_q = [&](const Seg& sg, bool first) {
                 const bool row_ok = i < a.n_h;
                 const uint4* src = reinterpret_cast<const uint4*>(a.qp + ((int64_t)sg.b * a.n_h + (row_ok ? i : 0)) * kRowElems);
                 const uint4 zero = make_uint4(0, 0, 0, 0);
                 {   // rotary columns [512 + 32r, 512 + 32r + 32): the A operand of the rotary
-                    // score MMAs, in shared memory (row i: 64 bytes, 16-byte chunk c stored at
-                    // chunk c ^ ((i >> 1) & 3), the 64B swizzle)
+                    // score MMAs (row i: 64 bytes, 16-byte chunk c stored at chunk
+                    // c ^ ((i >> 1) & 3), the 64B swizzle)
                     uint8_t* qrow = sm + kOffQR + i * 64;
     #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -650,21 +689,21 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     mbar_arrive(bar(B_QFULL));
                     return;
                 }
-                // latent columns [256r, 256r + 256) into tensor memory, two chunks of 64 bf16
-                // (32 TMEM columns each) per round of loads
-    #pragma unroll 1
-                for (int k = 0; k < 4; k += 2) {
+                {   // latent chunks 0, 1 (columns [256r, 256r + 128)) into tensor memory
                     uint32_t r0[32], r1[32];
     #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const uint4 v = row_ok ? src[rank * 32 + 8 * k + c] : zero;
-                        const uint4 w = row_ok ? src[rank * 32 + 8 * k + 8 + c] : zero;
+                        const uint4 v = row_ok ? src[rank * 32 + c] : zero;
+                        const uint4 w = row_ok ? src[rank * 32 + 8 + c] : zero;
                         r0[4 * c] = v.x; r0[4 * c + 1] = v.y; r0[4 * c + 2] = v.z; r0[4 * c + 3] = v.w;
                         r1[4 * c] = w.x; r1[4 * c + 1] = w.y; r1[4 * c + 2] = w.z; r1[4 * c + 3] = w.w;
                     }
-                    tmem_st32u(tmem + lane_base + kColQ + 32 * k, r0);
-                    tmem_st32u(tmem + lane_base + kColQ + 32 * k + 32, r1);
+                    tmem_st32u(tmem + lane_base + kColQ, r0);
+                    tmem_st32u(tmem + lane_base + kColQ + 32, r1);
                 }
+                // latent chunks 2, 3 (columns [256r + 128, 256r + 256)) into shared memory
+                store_ql_row(sm + kOffQL, i, row_ok ? src + rank * 32 + 16 : nullptr);
+                fence_proxy_async_smem();
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive_cnt(bar(B_QFULL), 3);

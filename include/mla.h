@@ -71,6 +71,9 @@ typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
 #define MLA_DEV_BAD_LENGTH   0x1  /* decode: seq_len[b] < 1; that sequence's outputs are zero, lse -inf */
 #define MLA_DEV_BAD_POSITION 0x2  /* append: pos0[b] < 0 or pos0[b] + n_new > cap[b]; rows of b not written */
 #define MLA_DEV_TIMEOUT      0x4  /* a bounded wait inside a kernel gave up; outputs undefined */
+#define MLA_DEV_SMEM_ALIGN   0x8  /* the attention kernel's dynamic shared memory did not start on a
+                                     1024-byte boundary (its swizzled tiles need one); it returned
+                                     without work, outputs undefined */
 
 typedef struct {
     int32_t n_heads;      /* n_h: attention heads */
