@@ -6,19 +6,21 @@
 // [256r, 256r+256) and rotary columns [512+32r, 512+32r+32) of every cache row, so
 // the pair streams each row from HBM exactly once.  Per tile of 64 rows:
 //
-//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=64 rows, K=288; the latent part
-//                            of Q'_r is the A operand in tensor memory, its rotary
-//                            part in shared memory; the cache tile is the B operand
+//   S_r = Q'_r C_r^T         tcgen05, M=128 heads, N=64 rows, K=288; Q'_r is the A
+//                            operand (latent columns 0-127 in tensor memory, columns
+//                            128-255 and the rotary part in shared memory); the cache
+//                            tile is the B operand
 //   S   = S_0 + S_1          each CTA sends its partial to the peer (DSMEM), as an
 //                            fp32 offset per head plus fp16 differences
 //   P   = exp2(S - m)        online softmax (identical in both CTAs; lazy max update)
-//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=64; P (bf16) from shared memory,
+//   O_r += P C_r[:, :256]    tcgen05, M=128, N=256, K=64; P (bf16) from tensor memory,
 //                            the cache tile read again as an MN-major B operand
 //
-// Tensor memory (512 columns): O_r 128 x 256 fp32, the latent part of Q'_r 128 x 256
-// bf16 (128 columns), S[2] 2 x 128 x 64 fp32 (one per tile parity).  Shared memory:
-// a 4-stage ring of cache tiles (about 147 KB in flight), two exchange buffers, P and
-// the rotary part of Q'_r.
+// Tensor memory (512 columns): O_r 128 x 256 fp32, latent columns 0-127 of Q'_r
+// (64 columns), P[2] 2 x 128 x 64 bf16 and S[2] 2 x 128 x 64 fp32 (one of each per tile
+// parity).  Shared memory: a 4-stage ring of cache tiles (about 147 KB in flight; one
+// TMA copy for a tile's latent half and one for its rotary half), two exchange buffers,
+// the rest of Q'_r, per-piece statistics.
 //
 // Warp roles: warp 0 TMA producer and exchange credits, warps 1 and 3 issue the score
 // MMAs of the even and odd tiles, warp 2 owns the tensor memory and issues the value
@@ -227,6 +229,16 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ uint64_t kdesc128(uint32_t a) { return smem_desc(a, 16, 1024, kSwizzle128B); }
 
+// One TMA copy of a 3-D box (x, y, z): here a tile's four 64-column latent chunks, which land as
+// four consecutive 64-row x 128-byte swizzled boxes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
 // Row i of Q'_r's latent chunks 2 and 3 into shared memory: two 128-head x 64-column bf16
 // chunks, K-major with the 128B swizzle (16-byte unit c of row i stored at unit c ^ (i & 7)).
 // src: the row's 16 uint4 (chunk 2 then chunk 3), or null for a zero row.
@@ -333,8 +345,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             // ------------------------------------------------------------ TMA producer + credits
             // One thread serves two queues in an event loop: TMA loads of cache tiles into
             // the ring, and the return of exchange buffers to the peer (a group that has read
-            // the peer's partial arrives on a local barrier; this thread, which has no remote
-            // stores of its own in flight, makes the cluster-scope release arrival).
+            // the peer's partial arrives on a local barrier; this thread passes the credit on
+            // with a relaxed remote arrival).  This thread paces the kernel: one copy per
+            // latent half tile, and no release fence behind the credit.
             if (lane == 0) {
                 TileIt<kTiled> ip, ic;                              // next tile to load, next credit
                 ip.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
@@ -359,8 +372,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                             const uint32_t dst = sStage + st * kStageBytes;
                             const int y = next_y;
                             mbar_expect_tx(bar(B_FULL + st), kStageBytes);
-                            for (int j = 0; j < 4; ++j)
-                                tma_load_2d(dst + j * kTBox, &map_c128, rank * kLatHalf + 64 * j, y, bar(B_FULL + st));
+                            tma_load_3d(dst, &map_c128, 0, y, (int)rank * 4, bar(B_FULL + st));
                             tma_load_2d(dst + 4 * kTBox, &map_c64, a.rope_x0 + rank * kRopeHalf, y, bar(B_FULL + st));
                             issued = T + 1;
                             mp = ip.next();
@@ -371,12 +383,17 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     if (mc) {
                         const uint32_t T = ic.T;
                         if (mbar_test_wait_cluster(bar(B_XCONS + (T & 1)), (T >> 1) & 1)) {
-                            mbar_arrive_remote(mapa(bar(B_XEMPTY + (T & 1)), peer));
+                            // no data is published by this signal (the reads of X are complete),
+                            // so no release: a release at cluster scope would wait for this
+                            // thread's copies in flight
+                            mbar_arrive_remote_relaxed(mapa(bar(B_XEMPTY + (T & 1)), peer));
                             mc = ic.next();
                             prog = true;
                         }
                     }
                     if (prog) {
+                        // (the clock read of an idle round also spaces the polls of the barriers,
+                        // which the arriving threads and the copy engine share)
                         t_prog = globaltimer_ns();
                     } else {
                         if (*abort_flag) break;
@@ -792,6 +809,18 @@ bool get_encoder() {
     return g_encode != nullptr;
 }
 
+// The latent columns as a 3-D tensor (64 columns, rows, 64-column chunks): one box of
+// 64 columns x kTok rows x 4 chunks is a tile's latent half.
+bool encode_latent_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t stride) {
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {stride * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTok, 4};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t stride, uint32_t bx,
                uint32_t by, CUtensorMapSwizzle sw) {
     cuuint64_t dims[2] = {cols, rows};
@@ -850,8 +879,7 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
     // latent boxes from kv; the rotary box from pe, or from kv after the latent when packed
     CUtensorMap mc128, mc64;
     const uint64_t kv_cols = cv.pe ? 512 : (uint64_t)kRowElems;
-    if (!encode_2d(&mc128, cv.kv, kv_cols, (uint64_t)cv.rows, (uint64_t)cv.kv_stride, 64, kTok,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (!encode_latent_3d(&mc128, cv.kv, kv_cols, (uint64_t)cv.rows, (uint64_t)cv.kv_stride) ||
         !encode_2d(&mc64, cv.pe ? cv.pe : cv.kv, cv.pe ? 64 : (uint64_t)kRowElems, (uint64_t)cv.rows,
                    (uint64_t)(cv.pe ? cv.pe_stride : cv.kv_stride), 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;

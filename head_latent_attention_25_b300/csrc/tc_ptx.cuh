@@ -52,6 +52,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
                  : "memory");
 }
 
+// The same without release semantics: for a signal that publishes no data of this thread
+// (for instance "a buffer the peer writes into has been read": the reads are complete).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
