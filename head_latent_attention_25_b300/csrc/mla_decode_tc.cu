@@ -22,14 +22,14 @@
 // TMA copy for a tile's latent half and one for its rotary half), two exchange buffers,
 // the rest of Q'_r, per-piece statistics.
 //
-// Warp roles: warp 0 TMA producer and exchange credits, warps 1 and 3 issue the score
+// Warp roles: warp 0 TMA producer, warps 1 and 3 issue the score
 // MMAs of the even and odd tiles, warp 2 owns the tensor memory and issues the value
 // MMAs, warps 4-7 and 8-11 two softmax/exchange groups that take alternate tiles
 // (thread i <-> head i <-> TMEM lane i), warps 12-15 load Q' of each piece and write
 // each piece's output.  Each group has its own exchange buffer, laid out [16-byte
 // chunk][head], so the 32 lanes of a warp write 512 contiguous bytes into the peer
 // (whole 32-byte sectors on the cluster interconnect); the peer's mbarrier counts the
-// bytes and a credit returns the buffer once the peer has read it.  Every wait is
+// bytes, and each warp that has read its rows returns a credit.  Every wait is
 // bounded in time; on expiry the CTA raises MLA_DEV_TIMEOUT, drains its own in-flight
 // copies and MMAs, frees TMEM and returns.
 #include <mutex>
@@ -85,8 +85,8 @@ static_assert(kOffQL % 1024 == 0 && kQLChunk % 1024 == 0, "swizzled operands nee
 enum : int {
     B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
     B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_VDONE = B_PFULL + 2, B_OFREE = B_VDONE + 2, B_XFULL,
-    B_XEMPTY = B_XFULL + 2, B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4, B_XCONS,
-    B_COUNT = B_XCONS + 2
+    B_XEMPTY = B_XFULL + 2, B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4,
+    B_COUNT = B_FIN + 1
 };
 static_assert(B_COUNT * 8 <= kBarBytes, "barrier area");
 constexpr uint32_t kOffTslot = kOffBar + kBarBytes;
@@ -305,8 +305,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
         mbar_init(bar(B_OFREE), 128);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_XFULL + i), 1);
-            mbar_init(bar(B_XEMPTY + i), 1);            // one credit from the peer's producer thread
-            mbar_init(bar(B_XCONS + i), 128);           // this CTA's group has read X[i]
+            mbar_init(bar(B_XEMPTY + i), 4);            // one credit from each warp of the peer's group
             mbar_init(bar(B_MH + i), 128);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(B_STATS + i), 256);
@@ -342,17 +341,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     if (active) {
         if (warp < 4) reg_alloc_dec<80>();
         if (warp == 0) {
-            // ------------------------------------------------------------ TMA producer + credits
-            // One thread serves two queues in an event loop: TMA loads of cache tiles into
-            // the ring, and the return of exchange buffers to the peer (a group that has read
-            // the peer's partial arrives on a local barrier; this thread passes the credit on
-            // with a relaxed remote arrival).  This thread paces the kernel: one copy per
-            // latent half tile, and no release fence behind the credit.
+            // ------------------------------------------------------------ TMA producer
+            // One thread loads the cache tiles into the ring: one copy for a tile's latent
+            // half and one for its rotary half.  (It paces the kernel; the exchange credits
+            // are sent by the softmax warps themselves.)
             if (lane == 0) {
-                TileIt<kTiled> ip, ic;                              // next tile to load, next credit
+                TileIt<kTiled> ip;                                  // next tile to load
                 ip.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
-                ic.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
-                bool mp = ip.next(), mc = ic.next();
+                bool mp = ip.next();
                 // cache row of the next tile to load, fetched one tile ahead (a block-table
                 // entry is a global load; its latency hides behind the wait for a free stage)
                 auto tile_row = [&](const TileIt<kTiled>& t) -> int {
@@ -364,9 +360,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 int next_y = mp ? tile_row(ip) : 0;
                 uint32_t issued = 0;
                 uint64_t t_prog = globaltimer_ns();
-                while (mp || mc) {
+                while (mp) {
                     bool prog = false;
-                    if (mp) {
+                    {
                         const uint32_t T = ip.T, st = T % kStages;
                         if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
                             const uint32_t dst = sStage + st * kStageBytes;
@@ -377,17 +373,6 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                             issued = T + 1;
                             mp = ip.next();
                             if (mp) next_y = tile_row(ip);
-                            prog = true;
-                        }
-                    }
-                    if (mc) {
-                        const uint32_t T = ic.T;
-                        if (mbar_test_wait_cluster(bar(B_XCONS + (T & 1)), (T >> 1) & 1)) {
-                            // no data is published by this signal (the reads of X are complete),
-                            // so no release: a release at cluster scope would wait for this
-                            // thread's copies in flight
-                            mbar_arrive_remote_relaxed(mapa(bar(B_XEMPTY + (T & 1)), peer));
-                            mc = ic.next();
                             prog = true;
                         }
                     }
@@ -582,7 +567,10 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                             }
                         }
                     }
-                    mbar_arrive(bar(B_XCONS + xb));
+                    // this warp has read its rows of X: pass the credit to the peer (relaxed, no
+                    // data is published; the loads above have returned)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote_relaxed(mapa(bar(B_XEMPTY + xb), peer));
                     // rows past the end of this piece do not count (only the last tile of a
                     // piece is partial)
                     const int valid = co.valid_rows();
