@@ -24,7 +24,7 @@ EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size"
             "mla_project_query_latent", "mla_query_latent_workspace_size",
             "mla_decode_absorbed_multi", "mla_decode_multi_workspace_size", "mla_project_output",
             "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size",
-            "mla_cache_append_ex", "mla_decode_absorbed_ex")
+            "mla_cache_append_ex", "mla_decode_absorbed_ex", "mla_copy_from_host")
 
 
 class MlaDims(ctypes.Structure):
@@ -107,6 +107,8 @@ def load():
     lib.mla_profile_events.restype = I32
     lib.mla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.mla_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.mla_copy_from_host.argtypes = [P, P, ctypes.c_size_t, P]
+    lib.mla_copy_from_host.restype = I32
     _lib = lib
     return lib
 
@@ -248,6 +250,12 @@ def mla_profile_events(start, stop):
             return e
         return e.cuda_event
     _check("mla_profile_events", load().mla_profile_events(h(start), h(stop)))
+
+
+def mla_copy_from_host(dst, src, nbytes: int, stream=None):
+    """dst: device buffer (tensor or pointer); src: page-locked host buffer (pinned tensor or
+    pointer); a kernel reads src over the bus (see include/mla.h)."""
+    _check("mla_copy_from_host", load().mla_copy_from_host(_p(dst), _p(src), int(nbytes), _stream(stream)))
 
 
 def mla_set_wait_limit_ns(ns: int) -> int:

@@ -67,11 +67,10 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile in
                                       uint64_t limit_ns) {
     if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    // the hardware may suspend the thread inside try_wait for up to the hint: never
-    // longer than the limit itself
-    const uint32_t hint = limit_ns < 20000u ? (uint32_t)limit_ns : 20000u;
+    // plain try_wait (no suspend-time hint): a thread suspended with a long hint was seen
+    // to wake late after the phase completed, which cost the short GEMMs of a step ~1 us
     while (true) {
-        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;

@@ -414,6 +414,24 @@ MLA_API mla_status mla_decode_absorbed_noalloc(const mla_dims* dims, mla_dtype d
  */
 MLA_API uint64_t mla_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * mla_copy_from_host -- copy `bytes` from page-locked host memory to device memory with a
+ * kernel that loads the host buffer directly over the bus (zero-copy reads), enqueued on
+ * `stream` (cudaStream_t as void*; NULL = the legacy default stream).  For staging a
+ * step's inputs in a serving loop: on hosts where a copy-engine transfer of a few MB pays
+ * a large fixed cost per call, this streams close to the link rate.  Transport plumbing
+ * of the library; the pages of the method have no counterpart.
+ *   dst    device memory (cudaMalloc or managed), `bytes` long, owned by the caller
+ *   src    host memory from cudaHostAlloc / cudaMallocHost / cudaHostRegister (page-locked
+ *          and mapped into the device's address space), owned by the caller; it must stay
+ *          valid and unchanged until the copy has run on `stream`
+ *   bytes  any size (16-byte aligned addresses and size take the wide path); 0 is a no-op
+ * Returns MLA_ERR_INVALID_ARG for a NULL pointer, a src that is not page-locked mapped host
+ * memory or a dst that is not device memory (checked with cudaPointerGetAttributes before
+ * any launch), MLA_ERR_CUDA if the launch fails.
+ */
+MLA_API mla_status mla_copy_from_host(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Static description of a status code (never NULL). */
 MLA_API const char* mla_status_string(mla_status status);
 
