@@ -418,13 +418,17 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& ma2, const CUtens
     if (a.staged && tile_bytes > ring) ring = (tile_bytes + 1023) / 1024 * 1024;
     a.off_bar = ring;
     const uint32_t smem = ring + 256 + 1024;
+    // Launched as a programmatic dependent of the kernel before it on the stream: the set-up
+    // (barriers, tensor memory) overlaps that kernel's tail, and the kernel waits for it
+    // (griddepcontrol.wait) before it reads any input.
     cudaError_t e;
 #define MLA_GEMM_CASE(NTV)                                                                         \
     case NTV: {                                                                                    \
         e = cudaFuncSetAttribute(gemm_tc_kernel<NTV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                  (int)smem);                                                      \
         if (e != cudaSuccess) return e;                                                           \
-        gemm_tc_kernel<NTV><<<grid, kGThreads, smem, s>>>(ma, ma2, mb, a);                         \
+        e = launch_ex(gemm_tc_kernel<NTV>, grid, dim3(kGThreads), smem, s, true, ma, ma2, mb, a);  \
+        if (e != cudaSuccess) return e;                                                           \
         break;                                                                                    \
     }
     switch (nt) {
