@@ -24,7 +24,8 @@ EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size"
             "mla_project_query_latent", "mla_query_latent_workspace_size",
             "mla_decode_absorbed_multi", "mla_decode_multi_workspace_size", "mla_project_output",
             "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size",
-            "mla_cache_append_ex", "mla_decode_absorbed_ex", "mla_copy_from_host")
+            "mla_cache_append_ex", "mla_decode_absorbed_ex", "mla_copy_from_host",
+            "mla_decode_prepare_beside")
 
 
 class MlaDims(ctypes.Structure):
@@ -92,7 +93,7 @@ def load():
     lib.mla_merge_output_weights.restype = I32
     lib.mla_output_workspace_size.argtypes = [D, I32, I32, I32]
     lib.mla_output_workspace_size.restype = SZ
-    for name in ("mla_decode_prepare", "mla_decode_attend"):
+    for name in ("mla_decode_prepare", "mla_decode_attend", "mla_decode_prepare_beside"):
         getattr(lib, name).argtypes = lib.mla_decode_absorbed.argtypes
         getattr(lib, name).restype = I32
     lib.mla_project_out.argtypes = [D, I32, I32, P, P, P, P, P]
@@ -209,6 +210,16 @@ def mla_decode_prepare(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, ro
                        stream=None):
     """First half of mla_decode_absorbed: query fold, q_R rotation, schedule (no cache reads)."""
     _check("mla_decode_prepare", load().mla_decode_prepare(
+        ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
+        _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
+        _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))
+
+
+def mla_decode_prepare_beside(dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len,
+                              max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                              stream=None):
+    """mla_decode_prepare that may run beside the kernel before it on the stream."""
+    _check("mla_decode_prepare_beside", load().mla_decode_prepare_beside(
         ctypes.byref(dims), dtype, batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows,
         _p(row_off), _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes,
         _p(o_lat), _p(lse), _p(dev_status), _stream(stream)))

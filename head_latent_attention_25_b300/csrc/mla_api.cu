@@ -295,7 +295,7 @@ size_t mla_decode_workspace_size(const mla_dims* dims, mla_dtype dtype, int32_t 
 
 namespace {
 
-enum : int { kPrepare = 1, kAttend = 2 };
+enum : int { kPrepare = 1, kAttend = 2, kBeside = 4 };
 
 // The decode in two phases: kPrepare (fold W_UK^T into the queries, rotate q_R, build the
 // schedule; reads no cache row) and kAttend (split-K attention over the cache, merge).
@@ -343,7 +343,7 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
             // fold GEMM, then q_R rotation and the schedule in one launch
             // the rotation and schedule kernel runs beside the fold GEMM (programmatic
             // dependent launch; it waits for the GEMM only at its end)
-            e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s);
+            e = launch_fold_tc(*dims, batch, q_c, w_uk, alpha, qp, dev_status, s, (phases & kBeside) != 0);
             if (e == cudaSuccess)
                 e = launch_fold_rope(*dims, true, true, batch, q_r, seq_len, alpha, qp, s, &sa, true);
         } else {
@@ -353,11 +353,10 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
     }
     if (e == cudaSuccess && (phases & kAttend)) {
         if (tc) {
-            // when this call also ran the prepare kernels, the attention kernel may start
-            // (set-up only) before the last of them ends
+            // the attention kernel may start (set-up only) before the kernel before it on the
+            // stream ends: it waits for that kernel before it reads anything
             e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cv, seq_len, row_off, cum,
-                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s,
-                                (phases & kPrepare) != 0);
+                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s, true);
         } else {
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
                                   sched, wstart, o_lat, lse, part_o, part_l, s);
@@ -483,6 +482,17 @@ mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t bat
                               void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
                               int32_t* dev_status, void* stream) {
     return decode_phases(kPrepare, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                         seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
+                         stream);
+}
+
+mla_status mla_decode_prepare_beside(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                                     const void* q_c, const void* q_r, const void* w_uk,
+                                     const void* cache, int64_t cache_rows, const int64_t* row_off,
+                                     const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                                     void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                     int32_t* dev_status, void* stream) {
+    return decode_phases(kPrepare | kBeside, dims, dtype, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
                          seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status,
                          stream);
 }

@@ -61,6 +61,8 @@ struct GemmTcArgs {
     float* part; int part_ld;         // fp32 partial: part[(split*N + t)*part_ld + m]
     int32_t* dev_status;
     uint64_t wait_ns;     // limit of every wait of the pipeline
+    int defer_wait;       // wait for the kernel before this one only at the end (it writes
+                          // nothing this one reads): the two run side by side
 };
 
 __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* st,
@@ -137,7 +139,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     // the kernel behind this one in the same call may be scheduled now (it waits for this
     // one's completion before it reads what this one writes)
     pdl_trigger();
-    pdl_wait();
+    if (!a.defer_wait) pdl_wait();
 
     if (warp == 0 && lane == 0) {
         // producer
@@ -258,6 +260,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // beside the kernel before it: this kernel's end implies that one's, for the kernels
+    // behind this one that wait for it
+    if (a.defer_wait) pdl_wait();
 }
 
 // cache row = [sum of partials for c ; RoPE(sum of partials for k_R, pos)] in bf16.
@@ -275,6 +280,7 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
                        const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
                        CacheView cv, int32_t* dev_status) {
     __shared__ float2 red[kFinGroups][kFinPairs];
+    pdl_trigger();              // a kernel behind this one may set up (it waits for this one to end)
     pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
     const int t = blockIdx.x;
     const int width = d_c + d_r;
@@ -664,7 +670,7 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
 }
 
 cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const void* w_uk, float alpha,
-                           void* qp, int32_t* dev_status, cudaStream_t s) {
+                           void* qp, int32_t* dev_status, cudaStream_t s, bool beside) {
     if (!encoder()) return cudaErrorNotSupported;
     const int nt = pick_nt(batch);
     const uint64_t dc = d.d_c, dh = d.d_h, nh = d.n_heads;
@@ -684,6 +690,7 @@ cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const 
     a.y_g = d.d_c + d.d_r;
     a.y_tok = (int64_t)d.n_heads * (d.d_c + d.d_r);
     a.dev_status = dev_status;
+    a.defer_wait = beside ? 1 : 0;
     return run_gemm(ma, ma, mb, a, d.n_heads, nt, s);
 }
 

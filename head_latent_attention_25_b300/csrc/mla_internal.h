@@ -65,8 +65,10 @@ cudaError_t launch_output_merged_tc(const mla_dims& d, int batch, const void* o_
                                     void* workspace, void* u, int32_t* dev_status, int sm_count, cudaStream_t s);
 cudaError_t launch_merge_output_weights_tc(const mla_dims& d, const void* w_o, const void* w_uv, void* w_ov,
                                            int32_t* dev_status, cudaStream_t s);
+// beside: the fold may run beside the kernel before it on the stream (that kernel writes
+// nothing it reads); it waits for that kernel only at its end
 cudaError_t launch_fold_tc(const mla_dims& d, int batch, const void* q_c, const void* w_uk, float alpha,
-                           void* qp, int32_t* dev_status, cudaStream_t s);
+                           void* qp, int32_t* dev_status, cudaStream_t s, bool beside = false);
 cudaError_t launch_project_out_tc(const mla_dims& d, int batch, const void* o_lat, const void* w_uv,
                                   void* out, int32_t* dev_status, cudaStream_t s);
 

@@ -232,9 +232,12 @@ class DecodeStep:
                 self.total_rows, self.row_off, self.seq_len, self.max_seq_len, self.num_splits,
                 self.workspace, self.workspace.numel(), self.o_lat, self.lse, self.dev_status)
 
-    def decode_prepare(self, stream=None):
-        """Query fold, q_R rotation and schedule into the workspace; reads no cache row."""
-        L.mla_decode_prepare(*self._decode_args(), stream)
+    def decode_prepare(self, stream=None, beside=False):
+        """Query fold, q_R rotation and schedule into the workspace; reads no cache row.
+
+        beside: the kernels may run beside the kernel enqueued before them on the stream
+        (the cache append, which writes nothing they read)."""
+        (L.mla_decode_prepare_beside if beside else L.mla_decode_prepare)(*self._decode_args(), stream)
 
     def decode_attend(self, stream=None):
         """Attention over the cache and merge, from what decode_prepare left in the workspace."""
@@ -265,11 +268,20 @@ class DecodeStep:
         """The whole path: append, [query projection], decode, up-projection.
 
         The cache append and the query-side half of the decode are independent (the fold
-        reads no cache row), so the append runs on a second stream beside it; the attention
-        waits for both.  Under stream capture this becomes two branches of the graph.
+        reads no cache row).  With the query given, both go on one stream and the fold runs
+        beside the append (mla_decode_prepare_beside: no fork and join, every launch chained
+        to the one before it).  With the query projected from h, the append runs on a second
+        stream beside the query projection and the fold; the attention waits for both.
+        Under stream capture the second form becomes two branches of the graph.
         """
         if self.n_q > 1 or self.cache_layout is not None:   # the decode is one call
             self.step_serial(stream)
+            return
+        if not self.query_from_h:
+            self.append(stream)
+            self.decode_prepare(stream, beside=True)
+            self.decode_attend(stream)
+            self.project_out(stream)
             return
         main = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(self.device)
         self.side.wait_stream(main)             # this step's inputs, and earlier reads of the cache

@@ -309,6 +309,23 @@ MLA_API mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int
                               const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
                               void* workspace, size_t workspace_bytes,
                               void* o_lat, float* lse, int32_t* dev_status, void* stream);
+/*
+ * mla_decode_prepare_beside -- mla_decode_prepare whose kernels may start while the
+ * kernel enqueued before it on `stream` is still running (for instance the cache append
+ * of the same step), so that the two run side by side on one stream.  The caller
+ * guarantees that the work before it on the stream writes none of what this call reads
+ * (q_c, q_r, w_uk, row_off, seq_len) and does not use `workspace`; every kernel of this
+ * call ends only after that earlier kernel has ended, so work enqueued behind it (such as
+ * mla_decode_attend) still sees everything before it complete.  Same arguments, errors
+ * and effect as mla_decode_prepare.  Launch scheduling of the library, no step of the
+ * method.
+ */
+MLA_API mla_status mla_decode_prepare_beside(const mla_dims* dims, mla_dtype dtype, int32_t batch,
+                              const void* q_c, const void* q_r, const void* w_uk,
+                              const void* cache, int64_t cache_rows, const int64_t* row_off,
+                              const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
+                              void* workspace, size_t workspace_bytes,
+                              void* o_lat, float* lse, int32_t* dev_status, void* stream);
 MLA_API mla_status mla_decode_attend(const mla_dims* dims, mla_dtype dtype, int32_t batch,
                              const void* q_c, const void* q_r, const void* w_uk,
                              const void* cache, int64_t cache_rows, const int64_t* row_off,
