@@ -42,6 +42,7 @@ __all__ = [
     "expand_heads", "full_keys", "decode_explicit", "decode_absorbed",
     "project_query", "project_out", "project_output", "merge_output_weights",
     "project_output_merged", "softmax_scale", "cache_elements_per_token", "cache_bytes",
+    "E4M3_MAX", "FP8_GROUP", "round_to_e4m3", "e4m3_value", "quantize_row_fp8", "dequantize_row_fp8",
 ]
 
 
@@ -283,3 +284,70 @@ def cache_bytes(elements_per_token: int, tokens: int, layers: int, bytes_per_val
     """Whole-cache bytes for one request ("DeepSeek MLA: 4 Attention Methods
     Compared", section "DeepSeek KV-cache memory comparison")."""
     return elements_per_token * tokens * layers * bytes_per_value
+
+
+# ---------------------------------------------------------------- fp8 latent cache
+# The pages name quantization among the things a cache layout may add ("The Journey to
+# Multi-Head Latent Attention", section "Memory savings do not automatically equal
+# latency savings") without fixing a format.  Reading taken here (the plainest one that
+# keeps the method's arithmetic): the latent part c of a row is stored as FP8 E4M3 codes
+# in groups of 128 columns, each group with one fp32 scale (its largest magnitude / 448,
+# so that the largest value maps to the largest finite code); the rotary part k_R stays
+# bf16, since it is small and carries the position.  A value is code * scale.
+
+E4M3_MAX = 448.0
+FP8_GROUP = 128
+
+
+def round_to_e4m3(x) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value, ties to even.
+
+    E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits, no infinities.  Normal
+    values 2^e (1 + f/8) for e in [-6, 8] (the largest finite, 2^8 * 1.75 = 448);
+    subnormals k 2^-9 for k = 1..7.  In the binade [2^e, 2^(e+1)) the spacing is 2^(e-3)
+    (below 2^-6 it stays 2^-9), so a value rounds to step * round_half_even(|x| / step).
+    Magnitudes above 448 saturate to 448.
+    """
+    a = np.asarray(x, dtype=np.float64)
+    m = np.abs(a)
+    _, p = np.frexp(np.where(m > 0, m, 1.0))        # m = f 2^p with f in [0.5, 1): binade e = p - 1
+    e = np.clip(p - 1, -6, 8)
+    step = np.ldexp(1.0, e - 3)
+    v = np.minimum(np.round(m / step) * step, E4M3_MAX)   # np.round: half to even
+    return np.copysign(v, a)
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """The value of FP8 E4M3 codes (uint8): sign s, exponent field E, fraction F give
+    (-1)^s 2^(E-7) (1 + F/8) for E > 0 and (-1)^s F 2^-9 for E = 0; codes 0x7F and 0xFF
+    (E = 15, F = 7) are NaN."""
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s, e, f = b >> 7, (b >> 3) & 15, b & 7
+    v = np.where(e > 0, np.ldexp(1.0 + f / 8.0, e - 7), np.ldexp(f.astype(np.float64), -9))
+    v = np.where((e == 15) & (f == 7), np.nan, v)
+    return np.where(s == 1, -v, v)
+
+
+def quantize_row_fp8(row, d_c: int, group: int = FP8_GROUP):
+    """A cache row [..., d_c + d_r] -> (values [..., d_c] on the E4M3 grid, scales
+    [..., d_c / group], rotary part [..., d_r] in bf16); value * scale is the stored latent.
+
+    The decision of each code is taken in fp32, the precision of the kernel that writes
+    the cache: scale = fp32(amax) / 448 and c / scale are fp32 divisions (round to
+    nearest), then rounded to E4M3.  A group of zeros gets scale 1.
+    """
+    r = f64(row)
+    c32 = r[..., :d_c].astype(np.float32)
+    g = c32.reshape(c32.shape[:-1] + (d_c // group, group))
+    amax = np.max(np.abs(g), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    y = (g / scale[..., None]).astype(np.float32)
+    vals = round_to_e4m3(y.astype(np.float64)).reshape(c32.shape)
+    return vals, scale.astype(np.float64), round_to_bf16(r[..., d_c:])
+
+
+def dequantize_row_fp8(values, scales, k_r, group: int = FP8_GROUP) -> np.ndarray:
+    """Rows [..., d_c + d_r] from quantize_row_fp8's parts: [values * scale ; k_R]."""
+    v = f64(values)
+    s = np.repeat(f64(scales), group, axis=-1)
+    return np.concatenate([v * s, f64(k_r)], axis=-1)

@@ -418,3 +418,61 @@ def test_empty_sequence_rejected():
     with pytest.raises(ValueError):
         mo.decode_explicit(np.zeros((1, 2)), np.zeros((1, 2)), np.zeros((1, 2, 3)),
                            np.zeros((1, 2, 3)), np.zeros((0, 5)), 10000.0)
+
+
+# ---------------------------------------------------------------- fp8 latent cache
+def test_pin_e4m3_rounding_matches_library_conversion():
+    """round_to_e4m3 against torch's float -> float8_e4m3fn conversion (round to nearest
+    even) on every representable value, every midpoint between neighbours (the ties) and
+    dense grids across the normal and subnormal ranges."""
+    torch = pytest.importorskip("torch")
+    vals = mo.e4m3_value(np.arange(256, dtype=np.uint8))
+    fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = (fin[:-1] + fin[1:]) / 2
+    grid = np.concatenate([fin, mids, np.linspace(-460, 460, 40001), np.geomspace(1e-6, 460, 4001),
+                           -np.geomspace(1e-6, 460, 4001)]).astype(np.float32)
+    ref = torch.from_numpy(grid).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = mo.round_to_e4m3(grid.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_pin_e4m3_decoding_matches_library_view():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = mo.e4m3_value(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    np.testing.assert_array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+    # closed forms: the largest finite value, the smallest normal and subnormal, signed zero
+    assert mo.e4m3_value(np.uint8(0x7E)) == 448.0
+    assert mo.e4m3_value(np.uint8(0x08)) == 2.0 ** -6
+    assert mo.e4m3_value(np.uint8(0x01)) == 2.0 ** -9
+    assert mo.e4m3_value(np.uint8(0x80)) == 0.0
+
+
+def test_pin_fp8_row_quantization():
+    """Each 128-column group: its largest magnitude lands on +-448 exactly, every value is
+    on the E4M3 grid and within half a grid step of c / scale, the rotary part is bf16,
+    and a group of zeros keeps scale 1."""
+    rng = np.random.default_rng(7)
+    d_c, d_r = 512, 64
+    row = rng.normal(0.0, 0.02, (3, d_c + d_r))
+    row[2, 128:256] = 0.0
+    vals, scales, k_r = mo.quantize_row_fp8(row, d_c)
+    assert vals.shape == (3, d_c) and scales.shape == (3, 4) and k_r.shape == (3, d_r)
+    g = vals.reshape(3, 4, 128)
+    for r in range(3):
+        for q in range(4):
+            if r == 2 and q == 1:
+                assert scales[r, q] == 1.0 and not g[r, q].any()
+                continue
+            assert np.max(np.abs(g[r, q])) == mo.E4M3_MAX
+    np.testing.assert_array_equal(mo.round_to_e4m3(vals), vals)
+    y = row[:, :d_c].astype(np.float32).astype(np.float64) / np.repeat(scales, 128, axis=1)
+    _, p = np.frexp(np.where(np.abs(y) > 0, np.abs(y), 1.0))
+    half_step = np.ldexp(1.0, np.clip(p - 1, -6, 8) - 4)
+    assert np.all(np.abs(vals - y) <= half_step * (1 + 1e-6))
+    np.testing.assert_array_equal(k_r, mo.round_to_bf16(row[:, d_c:]))
+    deq = mo.dequantize_row_fp8(vals, scales, k_r)
+    assert deq.shape == row.shape
+    assert np.max(np.abs(deq[:, :d_c] - row[:, :d_c])) <= 0.0625 * np.max(np.abs(row[:, :d_c]))
