@@ -25,7 +25,7 @@ EXPORTED = ("mla_cache_append", "mla_project_query", "mla_decode_workspace_size"
             "mla_decode_absorbed_multi", "mla_decode_multi_workspace_size", "mla_project_output",
             "mla_merge_output_weights", "mla_project_output_merged", "mla_output_workspace_size",
             "mla_cache_append_ex", "mla_decode_absorbed_ex", "mla_copy_from_host",
-            "mla_decode_prepare_beside")
+            "mla_decode_prepare_beside", "mla_cache_append_fp8", "mla_decode_absorbed_fp8")
 
 
 class MlaDims(ctypes.Structure):
@@ -108,6 +108,10 @@ def load():
     lib.mla_profile_events.restype = I32
     lib.mla_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.mla_set_wait_limit_ns.restype = ctypes.c_uint64
+    lib.mla_cache_append_fp8.argtypes = [D, I32, I32, P, P, P, P, P, P, P, I64, P, SZ, P, P]
+    lib.mla_cache_append_fp8.restype = I32
+    lib.mla_decode_absorbed_fp8.argtypes = [D, I32, P, P, P, P, I64, P, P, I32, I32, P, SZ, P, P, P, P]
+    lib.mla_decode_absorbed_fp8.restype = I32
     lib.mla_copy_from_host.argtypes = [P, P, ctypes.c_size_t, P]
     lib.mla_copy_from_host.restype = I32
     _lib = lib
@@ -157,6 +161,28 @@ def mla_cache_append(dims, dtype, batch, n_new, h, w_dkv, w_kr, row_off, cap, po
         ctypes.byref(dims), dtype, batch, n_new, _p(h), _p(w_dkv), _p(w_kr), _p(row_off), _p(cap),
         _p(pos0), _p(cache), cache_rows, _p(workspace), workspace_bytes, _p(dev_status),
         _stream(stream)))
+
+
+def fp8_row_bytes(d_c: int, d_r: int) -> int:
+    """MLA_FP8_ROW_BYTES: E4M3 latent codes, one fp32 scale per 128 columns, bf16 rotary part."""
+    return d_c + 4 * (d_c // 128) + 2 * d_r
+
+
+def mla_cache_append_fp8(dims, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cache, cache_rows,
+                         workspace, workspace_bytes, dev_status, stream=None):
+    """mla_cache_append into the fp8 row layout (bf16 h and weights)."""
+    _check("mla_cache_append_fp8", load().mla_cache_append_fp8(
+        ctypes.byref(dims), batch, n_new, _p(h), _p(w_dkv), _p(w_kr), _p(row_off), _p(cap), _p(pos0),
+        _p(cache), cache_rows, _p(workspace), workspace_bytes, _p(dev_status), _stream(stream)))
+
+
+def mla_decode_absorbed_fp8(dims, batch, q_c, q_r, w_uk, cache, cache_rows, row_off, seq_len, max_seq_len,
+                            num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream=None):
+    """mla_decode_absorbed over an fp8 cache (bf16 queries, weights and o_lat)."""
+    _check("mla_decode_absorbed_fp8", load().mla_decode_absorbed_fp8(
+        ctypes.byref(dims), batch, _p(q_c), _p(q_r), _p(w_uk), _p(cache), cache_rows, _p(row_off),
+        _p(seq_len), max_seq_len, num_splits, _p(workspace), workspace_bytes, _p(o_lat), _p(lse),
+        _p(dev_status), _stream(stream)))
 
 
 def mla_project_query(dims, dtype, batch, d_in, x, w_uq, w_qr, q_c, q_r, dev_status, stream=None):

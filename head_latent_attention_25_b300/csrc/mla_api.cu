@@ -306,15 +306,19 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
                          const void* cache, int64_t cache_rows, const int64_t* row_off,
                          const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits,
                          void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
-                         int32_t* dev_status, void* stream, const CacheView* layout = nullptr) {
+                         int32_t* dev_status, void* stream, const CacheView* layout = nullptr,
+                         bool fp8 = false) {
     if (!dims_ok(dims) || !dtype_ok(dtype)) return MLA_ERR_INVALID_ARG;
+    if (fp8 && (dtype != MLA_BF16 || layout || dims->d_c % 128)) return MLA_ERR_UNSUPPORTED;
     if (batch < 1 || max_seq_len < 0 || num_splits < 0 || cache_rows < 1) return MLA_ERR_INVALID_ARG;
     if (!q_c || !q_r || !w_uk || !cache || (!row_off && !(layout && layout->block_table)) || !seq_len ||
         !o_lat || !dev_status)
         return MLA_ERR_INVALID_ARG;
-    const size_t row_bytes = (size_t)(dims->d_c + dims->d_r) * elt(dtype);
+    const size_t row_bytes = fp8 ? (size_t)kFp8RowBytes(dims->d_c, dims->d_r)
+                                 : (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
-    const bool tc = tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
+    // the fp8 layout runs on the CUDA-core kernel
+    const bool tc = !fp8 && tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
     if (!tc && !simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
     if (layout && !tc) return MLA_ERR_UNSUPPORTED;
     CacheView cv{cache, nullptr, dims->d_c + dims->d_r, 0, cache_rows, nullptr, 0, 0};
@@ -359,7 +363,7 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
                                 sched, wstart, o_lat, lse, part_o, part_l, dev_status, s, true);
         } else {
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
-                                  sched, wstart, o_lat, lse, part_o, part_l, s);
+                                  sched, wstart, o_lat, lse, part_o, part_l, s, fp8);
         }
         // the merge kernel follows the attention kernel of this same call (programmatic
         // dependent launch: it is scheduled early and waits for it)
@@ -473,6 +477,33 @@ mla_status mla_decode_absorbed_ex(const mla_dims* dims, mla_dtype dtype, int32_t
     if (st != MLA_OK) return st;
     return decode_phases(kPrepare | kAttend, dims, dtype, batch, q_c, q_r, w_uk, cv.kv, cv.rows, row_off, seq_len,
                          max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream, &cv);
+}
+
+mla_status mla_cache_append_fp8(const mla_dims* dims, int32_t batch, int32_t n_new, const void* h,
+                                const void* w_dkv, const void* w_kr, const int64_t* row_off, const int32_t* cap,
+                                const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims)) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || n_new < 1 || (int64_t)batch * n_new > (1LL << 30) || cache_rows < 1) return MLA_ERR_INVALID_ARG;
+    if (!h || !w_dkv || !w_kr || !row_off || !cap || !pos0 || !cache || !dev_status) return MLA_ERR_INVALID_ARG;
+    if (!tc_shape(dims, MLA_BF16) || !gemm_tc_shapes_ok(*dims) || dims->d_c % 128) return MLA_ERR_UNSUPPORTED;
+    if (!aligned(cache, 16) || kFp8RowBytes(dims->d_c, dims->d_r) % 16) return MLA_ERR_INVALID_ARG;
+    const int sms = sm_count();
+    const size_t need = append_tc_workspace(*dims, batch * n_new, nullptr, sms);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    if (!aligned(h, 16) || !aligned(w_dkv, 16) || !aligned(w_kr, 16)) return MLA_ERR_INVALID_ARG;
+    return cuda_status(launch_append_fp8_tc(*dims, batch, n_new, h, w_dkv, w_kr, row_off, cap, pos0, cache,
+                                            cache_rows, workspace, dev_status, sms, (cudaStream_t)stream));
+}
+
+mla_status mla_decode_absorbed_fp8(const mla_dims* dims, int32_t batch, const void* q_c, const void* q_r,
+                                   const void* w_uk, const void* cache, int64_t cache_rows, const int64_t* row_off,
+                                   const int32_t* seq_len, int32_t max_seq_len, int32_t num_splits, void* workspace,
+                                   size_t workspace_bytes, void* o_lat, float* lse, int32_t* dev_status,
+                                   void* stream) {
+    return decode_phases(kPrepare | kAttend, dims, MLA_BF16, batch, q_c, q_r, w_uk, cache, cache_rows, row_off,
+                         seq_len, max_seq_len, num_splits, workspace, workspace_bytes, o_lat, lse, dev_status, stream,
+                         nullptr, true);
 }
 
 mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int32_t batch,

@@ -98,6 +98,10 @@ __host__ __device__ __forceinline__ void worker_range(const Schedule& S, const i
 // Where the latent rows of the cache live (the tensor-core path): the latent part in kv,
 // the rotary part in pe (or packed after the latent in kv), and the row of position t of
 // sequence b either row_off[b] + t (contiguous) or from a block table (paged).
+// Bytes of one row of the fp8 cache layout: E4M3 codes of the latent, one fp32 scale per
+// 128 latent columns, the rotary part in bf16 (MLA_FP8_ROW_BYTES in the public header).
+__host__ __device__ constexpr int kFp8RowBytes(int d_c, int d_r) { return d_c + 4 * (d_c / 128) + 2 * d_r; }
+
 struct CacheView {
     const void* kv;
     const void* pe;                 // null: packed, the rotary part at column d_c of kv

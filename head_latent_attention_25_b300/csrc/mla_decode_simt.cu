@@ -7,6 +7,8 @@
 // an unnormalised latent accumulator, rescaled whenever m grows (online softmax).
 #include <math.h>
 
+#include <cuda_fp8.h>
+
 #include "mla_common.cuh"
 #include "mla_internal.h"
 #include "mla_schedule.cuh"
@@ -41,7 +43,20 @@ struct SplitArgs {
     int n_h, d_c, d_r, batch;
 };
 
-template <typename Tc>
+// Element k of a row of the fp8 cache layout: a latent code times its group's scale, or
+// the bf16 rotary value.
+__device__ __forceinline__ float ld_fp8_row(const uint8_t* row, int k, int d_c) {
+    if (k < d_c) {
+        __nv_fp8_e4m3 q;
+        q.__x = row[k];
+        return float(q) * *reinterpret_cast<const float*>(row + d_c + 4 * (k >> 7));
+    }
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(row + d_c + 4 * (d_c >> 7) + 2 * (k - d_c)));
+}
+
+// Tc: the cache element type (float or bf16 rows of d_c + d_r elements; the output o_lat
+// has the same type).  kFp8: the cache holds rows of the fp8 layout instead, o_lat is bf16.
+template <typename Tc, bool kFp8 = false>
 __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
     extern __shared__ float smem[];
     const int dq = a.d_c + a.d_r;
@@ -76,12 +91,15 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
 #pragma unroll
         for (int t = 0; t < kMaxColsPerLane; ++t) acc[t] = 0.f;
         const Tc* rows = cache + a.row_off[b] * dq;
+        const int rb = kFp8RowBytes(a.d_c, a.d_r);
+        const uint8_t* rows8 = (const uint8_t*)a.cache + a.row_off[b] * (int64_t)rb;
         for (int64_t r0 = r_lo; r0 < r_hi; r0 += kTileRows) {
             const int nr = (int)min((int64_t)kTileRows, r_hi - r0);
             __syncthreads();
             for (int e = tid; e < nr * dq; e += kWarps * 32) {
                 const int j = e / dq, k = e - j * dq;
-                tile[j * ts + k] = ld(rows + (r0 + j) * dq + k);
+                if constexpr (kFp8) tile[j * ts + k] = ld_fp8_row(rows8 + (r0 + j) * (int64_t)rb, k, a.d_c);
+                else tile[j * ts + k] = ld(rows + (r0 + j) * dq + k);
             }
             __syncthreads();
             if (!active) continue;
@@ -309,14 +327,20 @@ int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count) {
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
                               const void* sched, const int32_t* wstart, void* o_lat, float* lse,
-                              float* part_o, float* part_l, cudaStream_t s) {
+                              float* part_o, float* part_l, cudaStream_t s, bool fp8) {
     SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, wstart, o_lat, lse, part_o, part_l,
                 d.n_heads, d.d_c, d.d_r, batch};
     const int dq = d.d_c + d.d_r;
     const size_t smem = (size_t)(kTileRows * (dq + 1) + kWarps * dq) * sizeof(float);
     dim3 grid(workers, (d.n_heads + kWarps - 1) / kWarps);
     cudaError_t e;
-    if (bf16) {
+    if (fp8) {
+        e = cudaFuncSetAttribute(split_simt_kernel<__nv_bfloat16, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        profile_before_split(s);
+        split_simt_kernel<__nv_bfloat16, true><<<grid, kWarps * 32, smem, s>>>(a);
+    } else if (bf16) {
         e = cudaFuncSetAttribute(split_simt_kernel<__nv_bfloat16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

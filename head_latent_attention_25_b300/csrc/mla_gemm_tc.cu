@@ -16,6 +16,7 @@
 #include "tc_ptx.cuh"
 
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 
 namespace mla {
 namespace {
@@ -343,6 +344,77 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
     *(__nv_bfloat162*)dst = __floats2bfloat162_rn(v0, v1);
 }
 
+// The same row written in the fp8 layout (contiguous cache of rows of kFp8RowBytes(d_c, d_r)
+// bytes): the latent as E4M3 codes in 128-column groups with one fp32 scale each (largest
+// magnitude of the group / 448, 1 for a zero group), the rotary part rotated and kept in
+// bf16.  Grid (token, 128-column groups, the rotary part last): thread (x, y) of a block
+// adds splits y, y + kF8Groups, ... of pair x; the groups' sums are added in a fixed order,
+// and the y = 0 threads (two warps) find the group's largest magnitude and store the codes.
+constexpr int kF8Pairs = 64;
+constexpr int kF8Groups = 4;
+
+__global__ void __launch_bounds__(kF8Pairs * kF8Groups)
+append_finalize_fp8_kernel(const float* __restrict__ part, int k_splits, int n_tok, int n_new, int d_c,
+                           int d_r, double rope_r, const int64_t* __restrict__ row_off,
+                           const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
+                           uint8_t* __restrict__ cache, int64_t cache_rows, int32_t* dev_status) {
+    __shared__ float2 red[kF8Groups][kF8Pairs];
+    __shared__ float wmax[2];
+    pdl_trigger();              // a kernel behind this one may set up (it waits for this one to end)
+    pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
+    const int t = blockIdx.x;
+    const int width = d_c + d_r;
+    const int x = threadIdx.x % kF8Pairs, y = threadIdx.x / kF8Pairs;
+    const int e = 2 * (blockIdx.y * kF8Pairs + x);
+    const int b = t / n_new, j = t % n_new;
+    const int p0 = pos0[b];
+    const int64_t cp = cap[b];
+    const int64_t off = row_off[b];
+    const bool bad = p0 < 0 || (int64_t)p0 + n_new > cp || off < 0 || off + cp > cache_rows;
+    if (bad) {
+        if (blockIdx.y == 0 && threadIdx.x == 0) atomicOr(dev_status, MLA_DEV_BAD_POSITION);
+        return;
+    }
+    const int64_t row = off + p0 + j;
+    uint8_t* dst = cache + row * (int64_t)kFp8RowBytes(d_c, d_r);
+    float2 acc = make_float2(0.f, 0.f);
+    if (e < width) {
+        const float* p = part + (int64_t)t * width + e;
+        const int64_t split_stride = (int64_t)n_tok * width;
+        for (int sp = y; sp < k_splits; sp += kF8Groups) {
+            const float2 v = *reinterpret_cast<const float2*>(p + sp * split_stride);
+            acc.x += v.x;
+            acc.y += v.y;
+        }
+    }
+    red[y][x] = acc;
+    __syncthreads();
+    if (y != 0) return;                         // warps 0 and 1 go on (x = lane + 32 * warp)
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < kF8Groups; ++q) { v0 += red[q][x].x; v1 += red[q][x].y; }
+    if (e >= d_c) {                             // the rotary block: rotate, store bf16
+        if (e >= width) return;
+        float c, sn;
+        rope_cos_sin((int64_t)p0 + j, (e - d_c) >> 1, rope_r, &c, &sn);
+        const float r0 = v0 * c - v1 * sn, r1 = v0 * sn + v1 * c;
+        *(__nv_bfloat162*)(dst + d_c + 4 * (d_c / 128) + 2 * (e - d_c)) = __floats2bfloat162_rn(r0, r1);
+        return;
+    }
+    // a latent group of 128 columns: every one of the 64 threads holds a pair
+    float m = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    asm volatile("bar.sync 1, 64;" ::: "memory");    // the two warps of this group only
+    const float amax = fmaxf(wmax[0], wmax[1]);
+    const float scale = amax > 0.f ? amax / 448.f : 1.f;
+    const __nv_fp8x2_storage_t q2 = __nv_cvt_float2_to_fp8x2(make_float2(v0 / scale, v1 / scale), __NV_SATFINITE,
+                                                              __NV_E4M3);
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst + e) = q2;
+    if (x == 0) *reinterpret_cast<float*>(dst + d_c + 4 * blockIdx.y) = scale;
+}
+
 // y[t, e] = bf16(sum over splits of part[split, t, e]) for a split-K GEMM, summed in a
 // fixed order (8 thread groups per column pair, then a shared-memory reduction), so the
 // result does not depend on timing.  Grid (token, column-pair groups of kFinPairs).
@@ -665,6 +737,46 @@ cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void
     e = launch_ex(append_finalize_kernel, fin_grid, dim3(kFinPairs * kFinGroups), 0, s, true,
                   (const float*)workspace, splits, n_tok, n_new, d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
                   row_off, cap, pos0, cv, dev_status);
+    note_launch();
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_append_fp8_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
+                                 const void* w_kr, const int64_t* row_off, const int32_t* cap,
+                                 const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                                 int32_t* dev_status, int sm_count, cudaStream_t s) {
+    if (!encoder()) return cudaErrorNotSupported;
+    const int n_tok = batch * n_new;
+    int splits = 1;
+    append_tc_workspace(d, n_tok, &splits, sm_count);
+    const int width = d.d_c + d.d_r;
+    const int k_chunks = (d.hidden + kGK - 1) / kGK;
+    const int nt = pick_nt(n_tok);
+    CUtensorMap ma, ma2, mb;
+    const uint64_t H = d.hidden;
+    if (!map3(&ma, w_dkv, H, d.d_c, 1, H * 2, H * 2 * d.d_c, kGK, kGM, 1) ||
+        !map3(&ma2, w_kr, H, d.d_r, 1, H * 2, H * 2 * d.d_r, kGK, d.d_r, 1) ||
+        !map3(&mb, h, H, 1, n_tok, H * 2, H * 2, kGK, 1, nt))
+        return cudaErrorInvalidValue;
+    GemmTcArgs a = gblank();
+    a.M = width;
+    a.N = n_tok;
+    a.k_chunks = k_chunks;
+    a.k_splits = splits;
+    a.chunks_per_split = (k_chunks + splits - 1) / splits;
+    a.m_split_tile = d.d_c / kGM;
+    a.a2_rows = d.d_r;
+    a.mode = kOutPartial;
+    a.part = (float*)workspace;
+    a.part_ld = width;
+    a.dev_status = dev_status;
+    cudaError_t e = run_gemm(ma, ma2, mb, a, 1, nt, s);
+    if (e != cudaSuccess) return e;
+    // one block per 128 latent columns, and one for the rotary part
+    const dim3 fin_grid(n_tok, d.d_c / 128 + (d.d_r / 2 + kF8Pairs - 1) / kF8Pairs);
+    e = launch_ex(append_finalize_fp8_kernel, fin_grid, dim3(kF8Pairs * kF8Groups), 0, s, true,
+                  (const float*)workspace, splits, n_tok, n_new, d.d_c, d.d_r, rope_ratio(d.rope_base, d.d_r),
+                  row_off, cap, pos0, (uint8_t*)cache, cache_rows, dev_status);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -43,6 +43,11 @@ cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int
 bool gemm_tc_shapes_ok(const mla_dims& d);
 size_t append_tc_workspace(const mla_dims& d, int n_tok, int* k_splits_out, int sm_count);
 struct CacheView;
+// the append into the fp8 cache layout (contiguous rows of kFp8RowBytes bytes)
+cudaError_t launch_append_fp8_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
+                                 const void* w_kr, const int64_t* row_off, const int32_t* cap,
+                                 const int32_t* pos0, void* cache, int64_t cache_rows, void* workspace,
+                                 int32_t* dev_status, int sm_count, cudaStream_t s);
 cudaError_t launch_append_tc(const mla_dims& d, int batch, int n_new, const void* h, const void* w_dkv,
                              const void* w_kr, const int64_t* row_off, const int32_t* cap,
                              const int32_t* pos0, const CacheView& cv, void* workspace,
@@ -85,7 +90,7 @@ cudaError_t launch_expand_queries(const int64_t* row_off, const int32_t* seq_len
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
                               const void* sched, const int32_t* wstart, void* o_lat, float* lse,
-                              float* part_o, float* part_l, cudaStream_t s);
+                              float* part_o, float* part_l, cudaStream_t s, bool fp8 = false);
 
 // bf16 tcgen05 split kernel for d_c = 512, d_r = 64, n_heads <= 128 (2-CTA clusters).
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,

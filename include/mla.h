@@ -290,6 +290,43 @@ MLA_API size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype d
                                                int32_t n_q, int32_t max_seq_len, int32_t num_splits);
 
 /*
+ * fp8 latent cache.  The pages name quantization among the things a cache layout may add
+ * ("The Journey to Multi-Head Latent Attention", section "Memory savings do not
+ * automatically equal latency savings") without fixing a format; this library's reading:
+ * one contiguous row of MLA_FP8_ROW_BYTES(d_c, d_r) bytes per token,
+ *   bytes [0, d_c)                      FP8 E4M3 codes of the latent c, in groups of 128
+ *                                       columns
+ *   bytes [d_c, d_c + 4 d_c/128)        one fp32 scale per group: the group's largest |c|
+ *                                       / 448 (1 for a group of zeros); c = code * scale
+ *   bytes [d_c + 4 d_c/128, + 2 d_r)    the rotary part k_R in bf16
+ * (DeepSeek-V3 shapes: 512 + 16 + 128 = 656 bytes, against 1,152 for a bf16 row).  Rows
+ * are addressed like the packed contiguous cache: token t of sequence b is row
+ * row_off[b] + t.  Requires d_c % 128 == 0 and a row size that is a multiple of 16.
+ *
+ * mla_cache_append_fp8 -- mla_cache_append (bf16 h and weights, tensor-core shapes) that
+ *   writes fp8 rows: the fp32 row is formed exactly as for a bf16 cache, then each group's
+ *   codes are taken in fp32 (x / scale, rounded to nearest even, saturating at 448).
+ *   workspace: mla_append_workspace_size(dims, MLA_BF16, batch, n_new) bytes.
+ * mla_decode_absorbed_fp8 -- mla_decode_absorbed over an fp8 cache (bf16 queries, weights
+ *   and o_lat); the attention runs on CUDA cores, each row decoded to fp32 (code * scale)
+ *   as it is read.  workspace: mla_decode_workspace_size(dims, MLA_BF16, ...) bytes.
+ * Arguments, errors and dev_status flags otherwise as for the bf16 calls; MLA_ERR_UNSUPPORTED
+ * for shapes outside the above.
+ */
+#define MLA_FP8_ROW_BYTES(d_c, d_r) ((d_c) + 4 * ((d_c) / 128) + 2 * (d_r))
+MLA_API mla_status mla_cache_append_fp8(const mla_dims* dims, int32_t batch, int32_t n_new, const void* h,
+                                        const void* w_dkv, const void* w_kr, const int64_t* row_off,
+                                        const int32_t* cap, const int32_t* pos0, void* cache, int64_t cache_rows,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                        void* stream);
+MLA_API mla_status mla_decode_absorbed_fp8(const mla_dims* dims, int32_t batch, const void* q_c,
+                                           const void* q_r, const void* w_uk, const void* cache,
+                                           int64_t cache_rows, const int64_t* row_off, const int32_t* seq_len,
+                                           int32_t max_seq_len, int32_t num_splits, void* workspace,
+                                           size_t workspace_bytes, void* o_lat, float* lse, int32_t* dev_status,
+                                           void* stream);
+
+/*
  * mla_decode_prepare, mla_decode_attend -- mla_decode_absorbed in two calls, so that the
  * query-side work can run beside the cache append of the same step (the fold reads no
  * cache row).  Both take exactly the arguments of mla_decode_absorbed, and the two calls
