@@ -291,7 +291,7 @@ MLA_API size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype d
 
 /*
  * fp8 latent cache.  The pages name quantization among the things a cache layout may add
- * ("The Journey to Multi-Head Latent Attention", section "Memory savings do not
+ * ("DeepSeek MLA: 4 Attention Methods Compared", section "Memory savings do not
  * automatically equal latency savings") without fixing a format; this library's reading:
  * one contiguous row of MLA_FP8_ROW_BYTES(d_c, d_r) bytes per token,
  *   bytes [0, d_c)                      FP8 E4M3 codes of the latent c, in groups of 128

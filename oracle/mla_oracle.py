@@ -287,8 +287,8 @@ def cache_bytes(elements_per_token: int, tokens: int, layers: int, bytes_per_val
 
 
 # ---------------------------------------------------------------- fp8 latent cache
-# The pages name quantization among the things a cache layout may add ("The Journey to
-# Multi-Head Latent Attention", section "Memory savings do not automatically equal
+# The pages name quantization among the things a cache layout may add ("DeepSeek MLA: 4
+# Attention Methods Compared", section "Memory savings do not automatically equal
 # latency savings") without fixing a format.  Reading taken here (the plainest one that
 # keeps the method's arithmetic): the latent part c of a row is stored as FP8 E4M3 codes
 # in groups of 128 columns, each group with one fp32 scale (its largest magnitude / 448,
