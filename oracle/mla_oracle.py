@@ -291,9 +291,10 @@ def cache_bytes(elements_per_token: int, tokens: int, layers: int, bytes_per_val
 # Attention Methods Compared", section "Memory savings do not automatically equal
 # latency savings") without fixing a format.  Reading taken here (the plainest one that
 # keeps the method's arithmetic): the latent part c of a row is stored as FP8 E4M3 codes
-# in groups of 128 columns, each group with one fp32 scale (its largest magnitude / 448,
-# so that the largest value maps to the largest finite code); the rotary part k_R stays
-# bf16, since it is small and carries the position.  A value is code * scale.
+# in groups of 128 columns, each group with one scale, a power of two stored as fp32 (the
+# smallest 2^k with largest magnitude / 2^k <= 448, as in microscaling formats), so that
+# code * scale is exact in bf16 as well; the rotary part k_R stays bf16, since it is small
+# and carries the position.  A value is code * scale.
 
 E4M3_MAX = 448.0
 FP8_GROUP = 128
@@ -332,18 +333,22 @@ def quantize_row_fp8(row, d_c: int, group: int = FP8_GROUP):
     """A cache row [..., d_c + d_r] -> (values [..., d_c] on the E4M3 grid, scales
     [..., d_c / group], rotary part [..., d_r] in bf16); value * scale is the stored latent.
 
-    The decision of each code is taken in fp32, the precision of the kernel that writes
-    the cache: scale = fp32(amax) / 448 and c / scale are fp32 divisions (round to
-    nearest), then rounded to E4M3.  A group of zeros gets scale 1.
+    The decisions are taken in fp32, the precision of the kernel that writes the cache:
+    q = fp32(amax) / 448 (an fp32 division), scale = 2^k with k the smallest integer such
+    that q <= 2^k (exact: from q's binary exponent), then c / scale (exact: a power of two)
+    rounded to E4M3.  A group of zeros gets scale 1.
     """
     r = f64(row)
     c32 = r[..., :d_c].astype(np.float32)
     g = c32.reshape(c32.shape[:-1] + (d_c // group, group))
     amax = np.max(np.abs(g), axis=-1)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    y = (g / scale[..., None]).astype(np.float32)
-    vals = round_to_e4m3(y.astype(np.float64)).reshape(c32.shape)
-    return vals, scale.astype(np.float64), round_to_bf16(r[..., d_c:])
+    q = (amax / np.float32(E4M3_MAX)).astype(np.float32).astype(np.float64)
+    m, e = np.frexp(np.where(q > 0, q, 1.0))          # q = m 2^e, m in [0.5, 1)
+    k = np.where(m == 0.5, e - 1, e)                   # q == 2^(e-1) exactly: that power itself
+    scale = np.where(q > 0, np.ldexp(1.0, k), 1.0)
+    y = g.astype(np.float64) / scale[..., None]
+    vals = round_to_e4m3(y).reshape(c32.shape)
+    return vals, scale, round_to_bf16(r[..., d_c:])
 
 
 def dequantize_row_fp8(values, scales, k_r, group: int = FP8_GROUP) -> np.ndarray:

@@ -451,9 +451,9 @@ def test_pin_e4m3_decoding_matches_library_view():
 
 
 def test_pin_fp8_row_quantization():
-    """Each 128-column group: its largest magnitude lands on +-448 exactly, every value is
-    on the E4M3 grid and within half a grid step of c / scale, the rotary part is bf16,
-    and a group of zeros keeps scale 1."""
+    """Each 128-column group: the scale is a power of two and the group's largest magnitude
+    lands in (224, 448], every value is on the E4M3 grid and within half a grid step of
+    c / scale, the rotary part is bf16, and a group of zeros keeps scale 1."""
     rng = np.random.default_rng(7)
     d_c, d_r = 512, 64
     row = rng.normal(0.0, 0.02, (3, d_c + d_r))
@@ -466,7 +466,13 @@ def test_pin_fp8_row_quantization():
             if r == 2 and q == 1:
                 assert scales[r, q] == 1.0 and not g[r, q].any()
                 continue
-            assert np.max(np.abs(g[r, q])) == mo.E4M3_MAX
+            sc = scales[r, q]
+            assert sc == 2.0 ** np.round(np.log2(sc))
+            # before rounding the group's largest |c| / scale lies in (224, 448]; on the grid
+            # it can round down onto 224
+            amax = np.max(np.abs(row[r, 128 * q:128 * q + 128].astype(np.float32).astype(np.float64)))
+            assert mo.E4M3_MAX / 2 < amax / sc <= mo.E4M3_MAX
+            assert mo.E4M3_MAX / 2 <= np.max(np.abs(g[r, q])) <= mo.E4M3_MAX
     np.testing.assert_array_equal(mo.round_to_e4m3(vals), vals)
     y = row[:, :d_c].astype(np.float32).astype(np.float64) / np.repeat(scales, 128, axis=1)
     _, p = np.frexp(np.where(np.abs(y) > 0, np.abs(y), 1.0))
