@@ -307,6 +307,62 @@ def time_from_h(args, name):
     return out
 
 
+def time_fp8_decode(args, name):
+    """The decode (fold, attention, merge) of the same batch and lengths over an fp8 cache
+    (E4M3 codes with power-of-two group scales, bf16 rotary part; seeded random codes) beside
+    the same decode over a bf16 cache (the workload's rows): mean of K launches each."""
+    import torch
+    import mla_inputs
+    from head_latent_attention_25_b300 import (fp8_row_bytes, make_dims, mla_decode_absorbed,
+                                               mla_decode_absorbed_fp8, mla_decode_workspace_size, runner,
+                                               MLA_BF16)
+    wl = mla_inputs.WORKLOADS[name]
+    st = runner.from_workload(wl, num_splits=args.num_splits)
+    st.step()
+    torch.cuda.synchronize()
+    rows = st.total_rows
+    rb = fp8_row_bytes(wl.d_c, wl.d_r)
+    g = torch.Generator(device="cuda").manual_seed(wl.seed)
+    cache8 = torch.empty(rows, rb, dtype=torch.uint8, device="cuda")
+    codes = torch.randint(0, 0x7E, (rows, wl.d_c), dtype=torch.uint8, device="cuda", generator=g)
+    signs = torch.randint(0, 2, (rows, wl.d_c), dtype=torch.uint8, device="cuda", generator=g) * 128
+    cache8[:, :wl.d_c] = codes | signs
+    cache8[:, wl.d_c:wl.d_c + 4 * (wl.d_c // 128)].view(torch.float32)[:] = 2.0 ** -14
+    cache8[:, wl.d_c + 4 * (wl.d_c // 128):].view(torch.bfloat16)[:] = st.cache[:rows, wl.d_c:]
+    dims = st.dims
+    ws_bytes = mla_decode_workspace_size(dims, MLA_BF16, st.batch, st.max_seq_len, args.num_splits)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    o8 = torch.empty_like(st.o_lat)
+    lse8 = torch.empty(st.batch, wl.n_heads, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    def fp8():
+        mla_decode_absorbed_fp8(dims, st.batch, st.q_c, st.q_r, st.w["w_uk"], cache8, rows, st.row_off,
+                                st.seq_len, st.max_seq_len, args.num_splits, ws, ws_bytes, o8, lse8, st.dev_status)
+
+    ms8, ms16 = timed(fp8), timed(st.decode)
+    assert int(st.dev_status.item()) == 0
+    out = {"workload": wl.name, "fp8_decode_ms": ms8, "bf16_decode_ms": ms16, "fp8_cache_bytes": rows * rb,
+           "bf16_cache_bytes": rows * (wl.d_c + wl.d_r) * 2,
+           "note": "fold + attention + merge; fp8 rows: E4M3 latent with power-of-two group scales, "
+                   "bf16 rotary part; codes turned into bf16 tiles in shared memory"}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_output_forms(args, name):
     """The layer output after the step, u = W_O [o_1; ...; o_n_h], timed two ways (mean of
     K launches each, CUDA events): two-step (W_UV per head, then W_O) and with W_UV merged
@@ -624,6 +680,7 @@ def run_ours(args, wl, rank, world):
     if wl.name in FROM_H and not args.no_from_h and not args.no_graph:
         line["h_to_o"] = time_from_h(args, FROM_H[wl.name])
         line["output_projection"] = time_output_forms(args, wl.name)
+        line["fp8_cache"] = time_fp8_decode(args, wl.name)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
     return line

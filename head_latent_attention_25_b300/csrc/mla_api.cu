@@ -317,8 +317,8 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
     const size_t row_bytes = fp8 ? (size_t)kFp8RowBytes(dims->d_c, dims->d_r)
                                  : (size_t)(dims->d_c + dims->d_r) * elt(dtype);
     if (!aligned(cache, 16) || row_bytes % 16) return MLA_ERR_INVALID_ARG;
-    // the fp8 layout runs on the CUDA-core kernel
-    const bool tc = !fp8 && tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
+    // the fp8 layout runs on the tensor-core kernel for its shapes, on CUDA cores otherwise
+    const bool tc = tc_shape(dims, dtype) && cache_rows >= 32 && cache_rows <= INT32_MAX;
     if (!tc && !simt_supported(dims)) return MLA_ERR_UNSUPPORTED;
     if (layout && !tc) return MLA_ERR_UNSUPPORTED;
     CacheView cv{cache, nullptr, dims->d_c + dims->d_r, 0, cache_rows, nullptr, 0, 0};
@@ -360,7 +360,7 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
             // the attention kernel may start (set-up only) before the kernel before it on the
             // stream ends: it waits for that kernel before it reads anything
             e = launch_split_tc(*dims, batch, p.workers, qp, p.q_rows, cv, seq_len, row_off, cum,
-                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s, true);
+                                sched, wstart, o_lat, lse, part_o, part_l, dev_status, s, true, fp8);
         } else {
             e = launch_split_simt(*dims, bf16, batch, p.workers, (const float*)qp, cache, row_off, cum,
                                   sched, wstart, o_lat, lse, part_o, part_l, s, fp8);

@@ -40,6 +40,7 @@
 
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 
 namespace mla {
 namespace {
@@ -86,9 +87,17 @@ enum : int {
     B_FULL = 0, B_EMPTY = B_FULL + kStages, B_QFULL = B_EMPTY + kStages, B_QEMPTY, B_SFULL,
     B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_VDONE = B_PFULL + 2, B_OFREE = B_VDONE + 2, B_XFULL,
     B_XEMPTY = B_XFULL + 2, B_MH = B_XEMPTY + 2, B_STATS = B_MH + 2, B_FIN = B_STATS + 4,
-    B_COUNT = B_FIN + 1
+    B_CONV = B_FIN + 1, B_CREAD = B_CONV + kStages, B_COUNT = B_CREAD + 1
 };
 static_assert(B_COUNT * 8 <= kBarBytes, "barrier area");
+
+// fp8 cache rows (kFp8): a stage receives the tile's E4M3 latent half (64 rows x 256 bytes)
+// in the upper half of its latent area, the rows' four fp32 group scales just below, and
+// the bf16 rotary half in its usual place; the epilogue warps then write the bf16 latent
+// chunks over the whole latent area (in place: every code and scale is read first).
+constexpr uint32_t kF8Codes = 16384;                     // stage offset of the codes
+constexpr uint32_t kF8Scales = 15360;                    // stage offset of the scales (16 B per row)
+constexpr uint32_t kF8StageTx = 64 * 256 + 64 * 16 + kTRope;
 constexpr uint32_t kOffTslot = kOffBar + kBarBytes;
 constexpr uint32_t kOffAbort = kOffTslot + 4;
 
@@ -265,10 +274,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-template <bool kTiled>
+// kTiled: paged cache (block table).  kFp8: rows of the fp8 layout (contiguous); map_c128
+// then covers the rows as bytes (box 256 x 64 rows), map_c64 the rotary bytes (64 x 64, 64B
+// swizzle) and map_sc the group scales (16 x 64); for bf16 rows map_sc is unused.
+template <bool kTiled, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_constant__ CUtensorMap map_c64,
-                TcArgs a) {
+                const __grid_constant__ CUtensorMap map_sc, TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
     if (smem_addr(sm) & 1023u) {        // the same in every CTA of the launch: all return here
@@ -288,7 +300,12 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     Ctl ctl{abort_flag, a.dev_status, a.wait_ns};
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) { mbar_init(bar(B_FULL + i), 1); mbar_init(bar(B_EMPTY + i), 1); }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_EMPTY + i), 1);
+            mbar_init(bar(B_CONV + i), 128);          // fp8: the epilogue warps converted stage i
+        }
+        mbar_init(bar(B_CREAD), 128);                 // fp8: every converter has read its codes
         // Q' of a piece is in place: the first piece's is loaded by the softmax groups (latent
         // part) and the epilogue warps (rotary part), later ones by the epilogue warps alone,
         // which then arrive three times each
@@ -367,9 +384,18 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                         if (mbar_test_wait(bar(B_EMPTY + st), ((T / kStages) & 1) ^ 1)) {
                             const uint32_t dst = sStage + st * kStageBytes;
                             const int y = next_y;
-                            mbar_expect_tx(bar(B_FULL + st), kStageBytes);
-                            tma_load_3d(dst, &map_c128, 0, y, (int)rank * 4, bar(B_FULL + st));
-                            tma_load_2d(dst + 4 * kTBox, &map_c64, a.rope_x0 + rank * kRopeHalf, y, bar(B_FULL + st));
+                            if constexpr (kFp8) {
+                                // codes of this CTA's latent half, the row's group scales, the
+                                // rotary half (bf16, 64B swizzle), all as bytes of the row
+                                mbar_expect_tx(bar(B_FULL + st), kF8StageTx);
+                                tma_load_2d(dst + kF8Codes, &map_c128, (int)rank * 256, y, bar(B_FULL + st));
+                                tma_load_2d(dst + kF8Scales, &map_sc, 512, y, bar(B_FULL + st));
+                                tma_load_2d(dst + 4 * kTBox, &map_c64, 528 + (int)rank * 64, y, bar(B_FULL + st));
+                            } else {
+                                mbar_expect_tx(bar(B_FULL + st), kStageBytes);
+                                tma_load_3d(dst, &map_c128, 0, y, (int)rank * 4, bar(B_FULL + st));
+                                tma_load_2d(dst + 4 * kTBox, &map_c64, a.rope_x0 + rank * kRopeHalf, y, bar(B_FULL + st));
+                            }
                             issued = T + 1;
                             mp = ip.next();
                             if (mp) next_y = tile_row(ip);
@@ -414,7 +440,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                     if (it.first_tile() && !(ok = wait<false>(bar(B_QFULL), it.si & 1, ctl))) break;
                     if ((T & 1u) == par) {
                         const uint32_t st = T % kStages;
-                        if (!(ok = wait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl))) break;
+                        if (!(ok = wait<false>(bar((kFp8 ? B_CONV : B_FULL) + st), (T / kStages) & 1, ctl))) break;
                         if (T >= 2 && !(ok = wait<false>(bar(B_SEMPTY + par), ((T >> 1) - 1) & 1, ctl))) break;
                         tc_fence_after();
                         const uint32_t stage = sStage + st * kStageBytes;
@@ -713,10 +739,59 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 tc_fence_before();
                 mbar_arrive_cnt(bar(B_QFULL), 3);
             };
+            // fp8 rows: turn the landed codes of tile T into the bf16 latent chunks the MMAs read.
+            // Thread i takes row i / 2, columns [128 (i % 2), +128) of this CTA's half (one
+            // group, one scale); all 128 read before any writes (CREAD), since the output
+            // covers the bytes the codes and scales landed in.
+            auto convert_tile = [&](uint32_t T) -> bool {
+                const uint32_t st = T % kStages;
+                if (!wwait<false>(bar(B_FULL + st), (T / kStages) & 1, ctl)) return false;
+                uint8_t* stage = sm + kOffStage + st * kStageBytes;
+                const int r = i >> 1, hh = i & 1;
+                const uint4* src = reinterpret_cast<const uint4*>(stage + kF8Codes + r * 256 + 128 * hh);
+                uint4 v[8];
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = src[c];
+                const float scale = reinterpret_cast<const float*>(stage + kF8Scales + r * 16)[2 * rank + hh];
+                mbar_arrive(bar(B_CREAD));
+                if (!wwait<false>(bar(B_CREAD), T & 1, ctl)) return false;
+                // code * scale is exact in bf16: the scale is a power of two (an integer-only
+                // form that adds the exponent to the code's bits measured slower than these
+                // conversions)
+    #pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};   // 16 codes, lowest column first
+                    uint32_t o[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)(w[e >> 1] >> (16 * (e & 1)));
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                        const float2 f = __half22float2(__half2(hr));
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+                        o[e] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    // columns 16c .. 16c + 15 of the thread's 128: chunk j, 16-byte units u, u + 1
+                    // (K-major, 128B swizzle: unit u of row r stored at unit u ^ (r & 7))
+                    const int col = 128 * hh + 16 * c;
+                    const int j = col >> 6, u = (col & 63) >> 3;
+                    uint8_t* rowp = stage + j * kTBox + r * 128;
+                    *(uint4*)(rowp + ((u ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *(uint4*)(rowp + (((u + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_CONV + st));
+                return true;
+            };
             bool ok = true;
             if (have) load_q(cur, true);
             while (ok && have) {
+                const uint32_t t_begin = t_end;
                 t_end += (uint32_t)tiles_of(cur);
+                if constexpr (kFp8) {
+                    // this piece's tiles first: its scores (and so the next piece's Q') wait for them
+                    for (uint32_t T = t_begin; ok && T < t_end; ++T) ok = convert_tile(T);
+                    if (!ok) break;
+                }
                 const bool more = walk.next(nxt);
                 if (more) {
                     // the score MMAs of this piece are done with Q'
@@ -809,6 +884,18 @@ bool encode_latent_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t r
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of bytes (the fp8 layout): cols bytes per row, rows rows of `stride` bytes, box bx x by.
+bool encode_u8(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t stride, uint32_t bx,
+               uint32_t by, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t box[2] = {bx, by};
+    cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t stride, uint32_t bx,
                uint32_t by, CUtensorMapSwizzle sw) {
     cuuint64_t dims[2] = {cols, rows};
@@ -833,13 +920,13 @@ int resident_pairs() {
     std::lock_guard<std::mutex> lock(mu);
     if (cache[dev] == 0) {
         int n = 0;
-        if (cudaFuncSetAttribute(split_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
+        if (cudaFuncSetAttribute(split_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) ==
             cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * 256);
             cfg.blockDim = dim3(kThreads);
             cfg.dynamicSmemBytes = kSmemBytes;
-            if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel<false>, &cfg) != cudaSuccess) n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel<false, false>, &cfg) != cudaSuccess) n = 0;
         }
         (void)cudaGetLastError();
         cache[dev] = n > 0 ? n : -1;
@@ -861,24 +948,37 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
                             int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             const int32_t* wstart, void* o_lat, float* lse, float* part_o,
-                            float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl) {
+                            float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl, bool fp8) {
     (void)q_rows;
     if (!get_encoder()) return cudaErrorNotSupported;
-    // latent boxes from kv; the rotary box from pe, or from kv after the latent when packed
-    CUtensorMap mc128, mc64;
-    const uint64_t kv_cols = cv.pe ? 512 : (uint64_t)kRowElems;
-    if (!encode_latent_3d(&mc128, cv.kv, kv_cols, (uint64_t)cv.rows, (uint64_t)cv.kv_stride) ||
-        !encode_2d(&mc64, cv.pe ? cv.pe : cv.kv, cv.pe ? 64 : (uint64_t)kRowElems, (uint64_t)cv.rows,
-                   (uint64_t)(cv.pe ? cv.pe_stride : cv.kv_stride), 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
-        return cudaErrorInvalidValue;
+    CUtensorMap mc128, mc64, msc;
+    if (fp8) {
+        // rows of the fp8 layout as bytes: this CTA's 256 codes, the 16 bytes of group scales,
+        // its 64 rotary bytes (64B swizzle, as the rotary score MMAs expect)
+        if (cv.block_table || cv.pe) return cudaErrorInvalidValue;
+        const uint64_t rb = (uint64_t)kFp8RowBytes(512, 64);
+        if (!encode_u8(&mc128, cv.kv, rb, (uint64_t)cv.rows, rb, 256, kTok, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_u8(&msc, cv.kv, rb, (uint64_t)cv.rows, rb, 16, kTok, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_u8(&mc64, cv.kv, rb, (uint64_t)cv.rows, rb, 64, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+    } else {
+        // latent boxes from kv; the rotary box from pe, or from kv after the latent when packed
+        const uint64_t kv_cols = cv.pe ? 512 : (uint64_t)kRowElems;
+        if (!encode_latent_3d(&mc128, cv.kv, kv_cols, (uint64_t)cv.rows, (uint64_t)cv.kv_stride) ||
+            !encode_2d(&mc64, cv.pe ? cv.pe : cv.kv, cv.pe ? 64 : (uint64_t)kRowElems, (uint64_t)cv.rows,
+                       (uint64_t)(cv.pe ? cv.pe_stride : cv.kv_stride), 32, kTok, CU_TENSOR_MAP_SWIZZLE_64B))
+            return cudaErrorInvalidValue;
+        msc = mc64;                                     // unused by the bf16 kernels
+    }
     TcArgs a{(const __nv_bfloat16*)qp, row_off, cv.block_table ? seq_len : nullptr, cv.block_table,
              cv.block_size, cv.max_blocks, cv.pe ? 0 : 512, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
              lse, part_o, part_l, dev_status, wait_limit_ns(), d.n_heads, batch};
-    auto kernel = cv.block_table ? split_tc_kernel<true> : split_tc_kernel<false>;
+    auto kernel = fp8 ? split_tc_kernel<false, true>
+                      : cv.block_table ? split_tc_kernel<true, false> : split_tc_kernel<false, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     profile_before_split(s);
-    e = launch_ex(kernel, dim3(2 * workers), dim3(kThreads), kSmemBytes, s, pdl, mc128, mc64, a);
+    e = launch_ex(kernel, dim3(2 * workers), dim3(kThreads), kSmemBytes, s, pdl, mc128, mc64, msc, a);
     profile_after_split(s);
     note_launch();
     return e != cudaSuccess ? e : cudaGetLastError();

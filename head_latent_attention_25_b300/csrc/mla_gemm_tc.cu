@@ -345,9 +345,9 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
 }
 
 // The same row written in the fp8 layout (contiguous cache of rows of kFp8RowBytes(d_c, d_r)
-// bytes): the latent as E4M3 codes in 128-column groups with one fp32 scale each (largest
-// magnitude of the group / 448, 1 for a zero group), the rotary part rotated and kept in
-// bf16.  Grid (token, 128-column groups, the rotary part last): thread (x, y) of a block
+// bytes): the latent as E4M3 codes in 128-column groups with one scale each, the smallest
+// power of two 2^k with (largest magnitude of the group) / 2^k <= 448 (1 for a zero
+// group), stored as fp32; the rotary part rotated and kept in bf16.  Grid (token, 128-column groups, the rotary part last): thread (x, y) of a block
 // adds splits y, y + kF8Groups, ... of pair x; the groups' sums are added in a fixed order,
 // and the y = 0 threads (two warps) find the group's largest magnitude and store the codes.
 constexpr int kF8Pairs = 64;
@@ -408,7 +408,14 @@ append_finalize_fp8_kernel(const float* __restrict__ part, int k_splits, int n_t
     if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
     asm volatile("bar.sync 1, 64;" ::: "memory");    // the two warps of this group only
     const float amax = fmaxf(wmax[0], wmax[1]);
-    const float scale = amax > 0.f ? amax / 448.f : 1.f;
+    // q = amax / 448 (fp32 division); 2^k is the smallest power of two >= q, read off q's
+    // binary exponent (q = m 2^e with m in [0.5, 1): k = e, or e - 1 when m = 0.5)
+    float scale = 1.f;
+    if (amax > 0.f) {
+        int e;
+        const float m = frexpf(amax / 448.f, &e);
+        scale = ldexpf(1.f, m == 0.5f ? e - 1 : e);
+    }
     const __nv_fp8x2_storage_t q2 = __nv_cvt_float2_to_fp8x2(make_float2(v0 / scale, v1 / scale), __NV_SATFINITE,
                                                               __NV_E4M3);
     *reinterpret_cast<__nv_fp8x2_storage_t*>(dst + e) = q2;

@@ -97,7 +97,7 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
                             int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
                             const int32_t* wstart, void* o_lat, float* lse, float* part_o,
-                            float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl);
+                            float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl, bool fp8 = false);
 
 // Combines the partial results of sequences cut across workers; zero-fills empty ones.
 cudaError_t launch_merge(const mla_dims& d, bool bf16, int batch, const int64_t* cum,

@@ -296,8 +296,9 @@ MLA_API size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype d
  * one contiguous row of MLA_FP8_ROW_BYTES(d_c, d_r) bytes per token,
  *   bytes [0, d_c)                      FP8 E4M3 codes of the latent c, in groups of 128
  *                                       columns
- *   bytes [d_c, d_c + 4 d_c/128)        one fp32 scale per group: the group's largest |c|
- *                                       / 448 (1 for a group of zeros); c = code * scale
+ *   bytes [d_c, d_c + 4 d_c/128)        one scale per group, stored as fp32: the smallest
+ *                                       power of two 2^k with the group's largest |c| /
+ *                                       2^k <= 448 (1 for a group of zeros); c = code * scale
  *   bytes [d_c + 4 d_c/128, + 2 d_r)    the rotary part k_R in bf16
  * (DeepSeek-V3 shapes: 512 + 16 + 128 = 656 bytes, against 1,152 for a bf16 row).  Rows
  * are addressed like the packed contiguous cache: token t of sequence b is row
@@ -305,11 +306,13 @@ MLA_API size_t mla_decode_multi_workspace_size(const mla_dims* dims, mla_dtype d
  *
  * mla_cache_append_fp8 -- mla_cache_append (bf16 h and weights, tensor-core shapes) that
  *   writes fp8 rows: the fp32 row is formed exactly as for a bf16 cache, then each group's
- *   codes are taken in fp32 (x / scale, rounded to nearest even, saturating at 448).
+ *   scale is found in fp32 and its codes are x / scale rounded to nearest even.
  *   workspace: mla_append_workspace_size(dims, MLA_BF16, batch, n_new) bytes.
  * mla_decode_absorbed_fp8 -- mla_decode_absorbed over an fp8 cache (bf16 queries, weights
- *   and o_lat); the attention runs on CUDA cores, each row decoded to fp32 (code * scale)
- *   as it is read.  workspace: mla_decode_workspace_size(dims, MLA_BF16, ...) bytes.
+ *   and o_lat).  For DeepSeek-V3 shapes (d_c = 512, d_r = 64, up to 128 heads, at least 32
+ *   cache rows) the attention runs on tensor cores: each landed tile's codes are turned into
+ *   bf16 (code * scale, exact since the scale is a power of two) in shared memory; otherwise
+ *   on CUDA cores.  workspace: mla_decode_workspace_size(dims, MLA_BF16, ...) bytes.
  * Arguments, errors and dev_status flags otherwise as for the bf16 calls; MLA_ERR_UNSUPPORTED
  * for shapes outside the above.
  */

@@ -1,4 +1,6 @@
-"""fp8 latent cache: append (tensor-core GEMM + fp8 finalize) and decode (CUDA cores).
+"""fp8 latent cache: append (tensor-core GEMM + fp8 finalize) and decode (tensor cores for
+DeepSeek-V3 shapes, with the codes turned into bf16 tiles in shared memory; CUDA cores for a
+cache of fewer than 32 rows).
 
 The appended rows are compared with the oracle's quantization of the oracle's own row
 (scales, codes within one grid step where the fp32 row and the fp64 row round differently,
@@ -41,27 +43,27 @@ def _decode_rows(raw):
     return vals, scales, kr
 
 
-def _setup(prefill, n_new, seed):
+def _setup(prefill, n_new, seed, n_h=N_H, extra_rows=7):
     L = _L()
     g = torch.Generator().manual_seed(seed)
     bf = torch.bfloat16
     w_dkv = (torch.randn(D_C, HIDDEN, generator=g) * 0.02).to(bf)
     w_kr = (torch.randn(D_R, HIDDEN, generator=g) * 0.02).to(bf)
-    w_uk = (torch.randn(N_H, D_H, D_C, generator=g) * 0.02).to(bf)
+    w_uk = (torch.randn(n_h, D_H, D_C, generator=g) * 0.02).to(bf)
     batch = len(prefill)
     h = torch.randn(batch * n_new, HIDDEN, generator=g).to(bf)
-    q_c = torch.randn(batch, N_H, D_H, generator=g).to(bf)
-    q_r = torch.randn(batch, N_H, D_R, generator=g).to(bf)
+    q_c = torch.randn(batch, n_h, D_H, generator=g).to(bf)
+    q_r = torch.randn(batch, n_h, D_R, generator=g).to(bf)
     cap = [p + n_new for p in prefill]
     row_off = np.concatenate([[0], np.cumsum(cap)[:-1]]).astype(np.int64)
-    rows_total = int(sum(cap)) + 7                       # a few rows past the last sequence
+    rows_total = int(sum(cap)) + extra_rows               # a few rows past the last sequence
     rb = L.fp8_row_bytes(D_C, D_R)
     # prefilled rows: random latents quantized by the oracle, encoded on the host
     pre = np.random.default_rng(seed).normal(0.0, 0.02, (rows_total, D_C + D_R))
     vals, scales, kr = mo.quantize_row_fp8(pre, D_C)
     host = _encode_rows(vals, scales, kr)
     assert host.shape == (rows_total, rb)
-    dims = L.make_dims(N_H, D_H, D_C, D_R, HIDDEN, BASE)
+    dims = L.make_dims(n_h, D_H, D_C, D_R, HIDDEN, BASE)
     dev = dict(
         w_dkv=w_dkv.cuda(), w_kr=w_kr.cuda(), w_uk=w_uk.cuda(), h=h.cuda(), q_c=q_c.cuda(), q_r=q_r.cuda(),
         cache=torch.from_numpy(host).cuda(), row_off=torch.from_numpy(row_off).cuda(),
@@ -109,31 +111,46 @@ def test_fp8_append_rows(prefill, n_new):
     np.testing.assert_array_equal(got[mask], host[mask])
 
 
-@pytest.mark.parametrize("num_splits", [0, 1, 3])
-def test_fp8_decode_matches_oracle_on_device_rows(num_splits):
-    prefill, n_new = [300, 129, 64, 1], 2
-    L, dims, dev, hostw, row_off, cap, host = _setup(prefill, n_new, seed=5)
+def _decode_and_compare(prefill, n_new, num_splits, n_h, seed, heads=None, extra_rows=7):
+    L, dims, dev, hostw, row_off, cap, host = _setup(prefill, n_new, seed, n_h=n_h, extra_rows=extra_rows)
     rows_total = host.shape[0]
     _append(L, dims, dev, n_new, rows_total)
     batch = len(prefill)
     max_len = max(cap)
     ws_bytes = L.mla_decode_workspace_size(dims, L.MLA_BF16, batch, max_len, num_splits)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    o_lat = torch.full((batch, N_H, D_C), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((batch, N_H), float("nan"), dtype=torch.float32, device="cuda")
+    o_lat = torch.full((batch, n_h, D_C), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((batch, n_h), float("nan"), dtype=torch.float32, device="cuda")
     L.mla_decode_absorbed_fp8(dims, batch, dev["q_c"], dev["q_r"], dev["w_uk"], dev["cache"], rows_total,
                               dev["row_off"], dev["seq_len"], max_len, num_splits, ws, ws_bytes, o_lat, lse,
                               dev["status"])
     torch.cuda.synchronize()
     assert int(dev["status"].item()) == 0
     got = dev["cache"].cpu().numpy()
-    w_uv = np.zeros((N_H, D_H, D_C))
+    hs = list(range(n_h)) if heads is None else heads
+    w_uv = np.zeros((len(hs), D_H, D_C))
     for b in range(batch):
         vals, scales, kr = _decode_rows(got[row_off[b]:row_off[b] + cap[b]])
         rows = mo.dequantize_row_fp8(vals, scales, kr)
-        ref = mo.decode_absorbed(hostw["q_c"][b], hostw["q_r"][b], hostw["w_uk"], w_uv, rows, BASE)
-        assert_parity(o_lat[b].cpu(), ref["o_lat"], "bf16", f"o_lat b={b}")
-        assert_parity(lse[b].cpu(), ref["lse"], "bf16", f"lse b={b}")
+        ref = mo.decode_absorbed(hostw["q_c"][b][hs], hostw["q_r"][b][hs], hostw["w_uk"][hs], w_uv, rows, BASE)
+        assert_parity(o_lat[b][hs].cpu(), ref["o_lat"], "bf16", f"o_lat b={b}")
+        assert_parity(lse[b][hs].cpu(), ref["lse"], "bf16", f"lse b={b}")
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_fp8_decode_matches_oracle_on_device_rows(num_splits):
+    """16 heads, ragged lengths with partial last tiles: the tensor-core kernel."""
+    _decode_and_compare([300, 129, 64, 1], 2, num_splits, N_H, seed=5)
+
+
+def test_fp8_decode_v3_heads_sampled():
+    """128 heads (DeepSeek-V3), several tiles per sequence, sampled heads against the oracle."""
+    _decode_and_compare([1500, 700, 4100], 1, 0, 128, seed=9, heads=[0, 1, 63, 64, 127])
+
+
+def test_fp8_decode_tiny_cache_cuda_cores():
+    """A cache of fewer than 32 rows runs on the CUDA-core kernel."""
+    _decode_and_compare([10, 3], 2, 0, N_H, seed=2, extra_rows=0)
 
 
 def test_fp8_append_bad_position_is_flagged_and_skipped():
