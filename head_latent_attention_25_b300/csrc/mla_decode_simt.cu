@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
                                                                  const float* __restrict__ part_l,
                                                                  Tout* __restrict__ o_lat,
                                                                  float* __restrict__ lse, int n_h, int d_c) {
+    pdl_trigger();                              // the kernel behind this one may set up
     pdl_wait();                                 // launched behind the split kernel
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31;
