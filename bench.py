@@ -681,6 +681,10 @@ def run_ours(args, wl, rank, world):
         line["h_to_o"] = time_from_h(args, FROM_H[wl.name])
         line["output_projection"] = time_output_forms(args, wl.name)
         line["fp8_cache"] = time_fp8_decode(args, wl.name)
+        # the decode alone (fold, attention, merge) beside the whole layer step of `value`
+        dec_ms = line["fp8_cache"]["bf16_decode_ms"]
+        line["decode_only"] = {"ms_per_step": dec_ms, "value": wl.batch * world / (dec_ms / 1e3), "unit": UNIT,
+                               "launch": "eager launches, mean of K"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
     return line
