@@ -39,7 +39,8 @@ def parse():
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="v3_b64_l4096")
+    p.add_argument("--workload", default="v3_b64_l4096",
+                   help="a named workload or one sweep point (v3_sweep_b<batch>_l<context>)")
     p.add_argument("--num-splits", type=int, default=0)
     p.add_argument("--sweep", action="store_true", help="one line per sweep point (not the contract line)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -758,7 +759,10 @@ def main():
     import mla_inputs
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    wl = mla_inputs.WORKLOADS[args.workload]
+    named = dict(mla_inputs.WORKLOADS, **{w.name: w for w in mla_inputs.sweep_workloads()})
+    if args.workload not in named:
+        raise SystemExit(f"unknown workload {args.workload!r}; known: {', '.join(named)}")
+    wl = named[args.workload]
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, wl)), flush=True)
