@@ -110,7 +110,7 @@ bool plan_decode(const mla_dims* d, mla_dtype t, int batch, int max_seq_len, int
     off = align_up(off + ws.cum_bytes, A);
     ws.sched_off = off; ws.sched_bytes = sizeof(Schedule);
     off = align_up(off + ws.sched_bytes, A);
-    ws.ws_off = off;    ws.ws_bytes = (size_t)w * sizeof(int32_t);
+    ws.ws_off = off;    ws.ws_bytes = (size_t)w * sizeof(WorkerStart);
     off = align_up(off + ws.ws_bytes, A);
     ws.po_off = off;    ws.po_bytes = (size_t)2 * w * d->n_heads * d->d_c * sizeof(float);
     off = align_up(off + ws.po_bytes, A);
@@ -332,7 +332,7 @@ mla_status decode_phases(int phases, const mla_dims* dims, mla_dtype dtype, int3
     void* qp = ws + p.ws.q_off;
     int64_t* cum = (int64_t*)(ws + p.ws.cum_off);
     void* sched = ws + p.ws.sched_off;
-    int32_t* wstart = (int32_t*)(ws + p.ws.ws_off);
+    WorkerStart* wstart = (WorkerStart*)(ws + p.ws.ws_off);
     float* part_o = (float*)(ws + p.ws.po_off);
     float* part_l = (float*)(ws + p.ws.pl_off);
     const bool bf16 = dtype == MLA_BF16;

@@ -95,6 +95,19 @@ __host__ __device__ __forceinline__ void worker_range(const Schedule& S, const i
     }
 }
 
+// Where worker g starts, written by the schedule kernel so that a decode kernel reaches its
+// first tile through one dependent load: the worker's range, its first sequence b (the
+// last one whose rows start at or before the range start), that sequence's span in the
+// flattened context and its first cache row.
+struct __align__(16) WorkerStart {
+    int64_t begin, end;     // rows [begin, end) of the flattened context (worker_range)
+    int64_t seq0, seq1;     // cum[b], cum[b + 1]
+    int64_t row0;           // row_off[b] for a contiguous cache, else 0
+    int32_t b;
+    int32_t pad;
+};
+static_assert(sizeof(WorkerStart) == 48, "three 16-byte loads");
+
 // Where the latent rows of the cache live (the tensor-core path): the latent part in kv,
 // the rotary part in pe (or packed after the latent in kv), and the row of position t of
 // sequence b either row_off[b] + t (contiguous) or from a block table (paged).

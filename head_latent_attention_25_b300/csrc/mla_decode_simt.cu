@@ -39,7 +39,7 @@ constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
 
 struct SplitArgs {
     const float* qp; const void* cache; const int64_t* row_off; const int64_t* cum;
-    const Schedule* sched; const int32_t* wstart; void* o_lat; float* lse; float* part_o; float* part_l;
+    const Schedule* sched; const WorkerStart* wstart; void* o_lat; float* lse; float* part_o; float* part_l;
     int n_h, d_c, d_r, batch;
 };
 
@@ -63,17 +63,16 @@ __global__ void __launch_bounds__(kWarps * 32) split_simt_kernel(SplitArgs a) {
     const int ts = dq + 1;                      // odd stride: lane j reading row j is conflict-free
     float* tile = smem;                         // [kTileRows][ts]
     float* qs = smem + kTileRows * ts;          // [kWarps][dq]
-    const Schedule S = *a.sched;
     const int g = blockIdx.x;
-    int64_t begin, end;
-    worker_range(S, a.cum, g, &begin, &end);
+    const WorkerStart W = a.wstart[g];
+    const int64_t begin = W.begin, end = W.end;
     if (begin >= end) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.y * kWarps + warp;
     const bool active = h < a.n_h;
     const Tc* cache = (const Tc*)a.cache;
 
-    int b = a.wstart[g];                        // last sequence whose rows start at or before begin
+    int b = W.b;                                // last sequence whose rows start at or before begin
     int64_t cur = begin;
     bool first = true;
     while (cur < end) {
@@ -327,7 +326,7 @@ int simt_workers(int batch, int n_heads, int64_t max_total_rows, int sm_count) {
 
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
-                              const void* sched, const int32_t* wstart, void* o_lat, float* lse,
+                              const void* sched, const WorkerStart* wstart, void* o_lat, float* lse,
                               float* part_o, float* part_l, cudaStream_t s, bool fp8) {
     SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, wstart, o_lat, lse, part_o, part_l,
                 d.n_heads, d.d_c, d.d_r, batch};

@@ -117,8 +117,7 @@ struct TcArgs {
     int32_t block_size, max_blocks;
     int32_t rope_x0;                   // column of the rotary part in its tensor map (512 packed, 0 split)
     const int64_t* cum;
-    const Schedule* sched;
-    const int32_t* wstart;             // first sequence of each worker's range
+    const WorkerStart* wstart;         // where each worker starts
     __nv_bfloat16* o_lat;
     float* lse;
     float* part_o;
@@ -142,26 +141,45 @@ struct Seg {
 // its length rounded up to a tile and its real length comes from real_len; the rows past
 // its length are never visited (range boundaries are tile-aligned).  A separate
 // instantiation keeps the contiguous walk free of that work.
-template <bool kTiled>
+// kKeep: the walk keeps the current sequence's span (its first one from the start record),
+// so its first piece needs no load of cum; the roles on the way to the first tile (the TMA
+// producer, the loaders of Q') use it, the others re-read cum and hold fewer registers.
+template <bool kTiled, bool kKeep = false>
 struct SegWalk {
     const int64_t* cum;
     const int32_t* real_len;
     int64_t cur, end;
+    int64_t seq0, seq1;                // cum[b], cum[b + 1]
     int b, g;
     bool first;
-    // start: the worker's first sequence, found by the schedule kernel
-    __device__ void init(const int64_t* c, const int32_t* rl, int start, int gi, const Schedule& S) {
+    // w: the worker's start record, written by the schedule kernel
+    __device__ void init(const int64_t* c, const int32_t* rl, const WorkerStart& w, int gi) {
         cum = c;
         real_len = rl;
         g = gi;
-        worker_range(S, c, gi, &cur, &end);
+        cur = w.begin;
+        end = w.end;
+        b = w.b;
+        if (kKeep) {
+            seq0 = w.seq0;
+            seq1 = w.seq1;
+        }
         first = true;
-        b = start;
     }
     __device__ bool next(Seg& s) {
         if (cur >= end) return false;
-        while (cum[b + 1] <= cur) ++b;
-        const int64_t seq0 = cum[b], span = cum[b + 1] - seq0;
+        if (kKeep) {
+            while (seq1 <= cur) {
+                ++b;
+                seq0 = seq1;
+                seq1 = cum[b + 1];
+            }
+        } else {
+            while (cum[b + 1] <= cur) ++b;
+            seq0 = cum[b];
+            seq1 = cum[b + 1];
+        }
+        const int64_t span = seq1 - seq0;
         s.b = b;
         s.len = kTiled ? min(span, (int64_t)real_len[b]) : span;
         s.lo = cur - seq0;
@@ -177,9 +195,9 @@ struct SegWalk {
 __device__ __forceinline__ int tiles_of(const Seg& s) { return (int)((s.hi - s.lo + kTok - 1) / kTok); }
 
 // The worker's tiles in order: global tile index T, piece index si, tile t of ntiles.
-template <bool kTiled>
+template <bool kTiled, bool kKeep = false>
 struct TileIt {
-    SegWalk<kTiled> walk;
+    SegWalk<kTiled, kKeep> walk;
     Seg seg;
     int t = -1, ntiles = 0;
     uint32_t T = 0xffffffffu, si = 0xffffffffu;
@@ -347,11 +365,9 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
     // dependent launch), the kernel waits here, so its set-up overlaps their tail.
     pdl_wait();
     pdl_trigger();                  // the merge kernel behind this one may be scheduled
-    const Schedule S = *a.sched;
     const int g = blockIdx.x >> 1;
-    int64_t r_begin, r_end;
-    worker_range(S, a.cum, g, &r_begin, &r_end);
-    const bool active = r_begin < r_end;               // the same for both CTAs of the pair
+    const WorkerStart W = a.wstart[g];                 // one load: range, first sequence and row
+    const bool active = W.begin < W.end;               // the same for both CTAs of the pair
 
     // Registers: 128 per thread at launch; each role re-sizes its warpgroup's share
     // first thing in its own branch (80 + 168 + 168 + 96 = 4 x 128).
@@ -363,14 +379,15 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             // half and one for its rotary half.  (It paces the kernel; the exchange credits
             // are sent by the softmax warps themselves.)
             if (lane == 0) {
-                TileIt<kTiled> ip;                                  // next tile to load
-                ip.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                TileIt<kTiled, true> ip;                            // next tile to load
+                ip.walk.init(a.cum, a.seq_len, W, g);
                 bool mp = ip.next();
                 // cache row of the next tile to load, fetched one tile ahead (a block-table
                 // entry is a global load; its latency hides behind the wait for a free stage)
-                auto tile_row = [&](const TileIt<kTiled>& t) -> int {
+                auto tile_row = [&](const TileIt<kTiled, true>& t) -> int {
                     const int64_t pos = t.seg.lo + (int64_t)t.t * kTok;
-                    if (!kTiled) return (int)(a.row_off[t.seg.b] + pos);      // contiguous
+                    if (!kTiled)                                              // contiguous
+                        return (int)((t.seg.b == W.b ? W.row0 : a.row_off[t.seg.b]) + pos);
                     return a.block_table[(int64_t)t.seg.b * a.max_blocks + pos / a.block_size] * a.block_size +
                            (int)(pos % a.block_size);
                 };
@@ -433,7 +450,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 const uint32_t id_s = idesc_bf16_f32(kHeads, kTok, 0, 0);
                 const uint32_t sQL = base + kOffQL, sQR = base + kOffQR;
                 TileIt<kTiled> it;
-                it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                it.walk.init(a.cum, a.seq_len, W, g);
                 bool ok = true;
                 while (ok && it.next()) {
                     const uint32_t T = it.T;
@@ -470,7 +487,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             if (lane == 0) {
                 const uint32_t id_o = idesc_bf16_f32(kHeads, kLatHalf, 0, 1);
                 TileIt<kTiled> it;
-                it.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                it.walk.init(a.cum, a.seq_len, W, g);
                 bool ok = true;
                 while (ok && it.next()) {
                     const uint32_t T = it.T, st = T % kStages;
@@ -509,8 +526,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 // into shared memory), one round of loads, while the epilogue warps load the
                 // rotary part (at the start of a launch the three warpgroups together cut the
                 // wait for Q')
-                SegWalk<kTiled> w0;
-                w0.init(a.cum, a.seq_len, a.wstart[g], g, S);
+                SegWalk<kTiled, true> w0;
+                w0.init(a.cum, a.seq_len, W, g);
                 Seg s0;
                 if (w0.next(s0)) {
                     const bool row_ok = i < a.n_h;
@@ -538,7 +555,7 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 }
             }
             TileIt<kTiled> co;
-            co.walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+            co.walk.init(a.cum, a.seq_len, W, g);
             bool ok = true;
             float m_g = -INFINITY, l_g = 0.f;
             while (ok && co.next()) {
@@ -693,8 +710,8 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
             reg_alloc_dec<96>();
             const int i = tid - 384;                        // head row == TMEM lane
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-            SegWalk<kTiled> walk;
-            walk.init(a.cum, a.seq_len, a.wstart[g], g, S);
+            SegWalk<kTiled, true> walk;
+            walk.init(a.cum, a.seq_len, W, g);
             Seg cur, nxt;
             bool have = walk.next(cur);
             uint32_t si = 0, t_end = 0;                     // piece index, global index past its last tile
@@ -947,9 +964,10 @@ int tc_workers(int64_t max_total_rows, int sm_count) {
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
                             int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
-                            const int32_t* wstart, void* o_lat, float* lse, float* part_o,
+                            const WorkerStart* wstart, void* o_lat, float* lse, float* part_o,
                             float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl, bool fp8) {
     (void)q_rows;
+    (void)sched;                                    // the kernel reads the start records instead
     if (!get_encoder()) return cudaErrorNotSupported;
     CUtensorMap mc128, mc64, msc;
     if (fp8) {
@@ -971,7 +989,7 @@ cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const voi
         msc = mc64;                                     // unused by the bf16 kernels
     }
     TcArgs a{(const __nv_bfloat16*)qp, row_off, cv.block_table ? seq_len : nullptr, cv.block_table,
-             cv.block_size, cv.max_blocks, cv.pe ? 0 : 512, cum, (const Schedule*)sched, wstart, (__nv_bfloat16*)o_lat,
+             cv.block_size, cv.max_blocks, cv.pe ? 0 : 512, cum, wstart, (__nv_bfloat16*)o_lat,
              lse, part_o, part_l, dev_status, wait_limit_ns(), d.n_heads, batch};
     auto kernel = fp8 ? split_tc_kernel<false, true>
                       : cv.block_table ? split_tc_kernel<true, false> : split_tc_kernel<false, false>;

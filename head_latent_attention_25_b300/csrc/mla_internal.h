@@ -33,6 +33,7 @@ cudaError_t launch_project_out(const mla_dims& d, bool bf16, int batch, const vo
 
 // The rotary part of Q' alone (the content part comes from a GEMM).
 struct ScheduleArgs;
+struct WorkerStart;
 // q_R rotation into Q'; with sched_args it also builds the split schedule (one extra
 // block column), otherwise launch_schedule does.
 cudaError_t launch_fold_rope(const mla_dims& d, bool in_bf16, bool out_bf16, int batch, const void* q_r,
@@ -89,14 +90,14 @@ cudaError_t launch_expand_queries(const int64_t* row_off, const int32_t* seq_len
 // fp32-Q' SIMT split kernel (any supported dims, fp32 or bf16 cache).
 cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int workers, const float* qp,
                               const void* cache, const int64_t* row_off, const int64_t* cum,
-                              const void* sched, const int32_t* wstart, void* o_lat, float* lse,
+                              const void* sched, const WorkerStart* wstart, void* o_lat, float* lse,
                               float* part_o, float* part_l, cudaStream_t s, bool fp8 = false);
 
 // bf16 tcgen05 split kernel for d_c = 512, d_r = 64, n_heads <= 128 (2-CTA clusters).
 cudaError_t launch_split_tc(const mla_dims& d, int batch, int workers, const void* qp,
                             int64_t q_rows, const CacheView& cv, const int32_t* seq_len,
                             const int64_t* row_off, const int64_t* cum, const void* sched,
-                            const int32_t* wstart, void* o_lat, float* lse, float* part_o,
+                            const WorkerStart* wstart, void* o_lat, float* lse, float* part_o,
                             float* part_l, int32_t* dev_status, cudaStream_t s, bool pdl, bool fp8 = false);
 
 // Combines the partial results of sequences cut across workers; zero-fills empty ones.

@@ -15,7 +15,7 @@ struct ScheduleArgs {
     int workers;
     int64_t* cum;           // [batch + 1]
     Schedule* sched;
-    int32_t* wstart;        // [workers]
+    WorkerStart* wstart;    // [workers]
     int32_t* dev_status;
     int align;              // sequences flattened in multiples of this many rows (1, or a tile for paged caches)
     int64_t paged_cap;      // > 0: paged cache, a sequence is usable when 1 <= seq_len <= paged_cap (row_off unused)
@@ -74,31 +74,40 @@ __device__ __forceinline__ void build_schedule(const ScheduleArgs& a) {
     // worker buys no cut sequence (no partial results, no merge, no mid-range reload of
     // the folded query).
     const bool whole = a.batch <= a.workers && (long long)longest <= per + per / 4;
+    Schedule s;
+    s.total = total;
+    s.workers = a.workers;
+    s.batch = a.batch;
+    s.per = per;
+    s.whole = whole ? 1 : 0;
     if (tid == 0) {
         a.cum[0] = 0;
-        Schedule s;
-        s.total = total;
-        s.workers = a.workers;
-        s.batch = a.batch;
-        s.per = per;
-        s.whole = whole ? 1 : 0;
         *a.sched = s;
     }
     __syncthreads();                            // cum complete and visible to the block
-    // first sequence of each worker's range: the last sequence whose rows start at or
-    // before the range start (saves every role of the split kernels a binary search)
+    // each worker's start: its range, and its first sequence, the last one whose rows start
+    // at or before the range start (saves every role of the split kernels a binary search
+    // and the loads of a walk to its first tile)
     for (int g = tid; g < a.workers; g += nt) {
+        WorkerStart w;
+        worker_range(s, a.cum, g, &w.begin, &w.end);
+        int b;
         if (whole) {
-            a.wstart[g] = g < a.batch ? g : a.batch - 1;
-            continue;
+            b = g < a.batch ? g : a.batch - 1;
+        } else {
+            int lo = 0, hi = a.batch - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.cum[mid] <= w.begin) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
         }
-        const int64_t cur = (int64_t)g * per;
-        int lo = 0, hi = a.batch - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.cum[mid] <= cur) lo = mid; else hi = mid - 1;
-        }
-        a.wstart[g] = lo;
+        w.b = b;
+        w.pad = 0;
+        w.seq0 = a.cum[b];
+        w.seq1 = a.cum[b + 1];
+        w.row0 = (a.paged_cap > 0 || a.row_off == nullptr) ? 0 : a.row_off[b];
+        a.wstart[g] = w;
     }
 }
 
