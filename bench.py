@@ -29,7 +29,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode tokens/s (1 B300) and latent-cache HBM GB/s as % of roofline"
 UNIT = "tokens/s"
 DOMINANT_KERNEL_SOURCES = ["head_latent_attention_25_b300/csrc/mla_decode_tc.cu",
-                           "head_latent_attention_25_b300/csrc/tc_ptx.cuh"]
+                           "head_latent_attention_25_b300/csrc/tc_ptx.cuh",
+                           "head_latent_attention_25_b300/csrc/mla_common.cuh"]
 DOMINANT_KERNEL_NAME = "split_tc_kernel"
 
 
