@@ -175,8 +175,12 @@ __device__ __forceinline__ int64_t piece_slot(int64_t w, int64_t seq_begin, int6
     return 2 * w + (seq_begin <= w * per ? 0 : 1);
 }
 
+// Wide column chunks (kCols = 16, the many-sequence grids) hold 8 float4 loads a lane in
+// flight and at most 85 registers, so three blocks fit on an SM (the grid's blocks start in
+// fewer waves once the split kernel frees the SMs); narrow chunks (kCols = 4, a few long
+// sequences cut in many pieces) keep 16 loads a lane in flight and two blocks an SM.
 template <typename Tout, int kCols>
-__global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* __restrict__ cum,
+__global__ void __launch_bounds__(32 * kMergeHeads, kCols == 16 ? 3 : 2) merge_kernel(const int64_t* __restrict__ cum,
                                                                  const Schedule* __restrict__ sched,
                                                                  const float* __restrict__ part_o,
                                                                  const float* __restrict__ part_l,
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(32 * kMergeHeads) merge_kernel(const int64_t* 
     const float inv = 1.f / L;
     if (lane == 0 && lse && blockIdx.z == 0) lse[(int64_t)b * n_h + h] = (mx + log2f(L)) * kLn2;
     // pass 2: in round rd a lane owns columns [kCols lane, kCols lane + kCols) + 32 kCols rd
-    constexpr int kIn = 64 / kCols;             // pieces in flight (16 float4 loads a lane)
+    constexpr int kIn = (kCols == 16 ? 32 : 64) / kCols;   // pieces in flight
     const bool vec = (d_c % kCols) == 0;        // float4 loads stay aligned
     const int rounds = (d_c + 32 * kCols - 1) / (32 * kCols);
     for (int rd = blockIdx.z; rd < rounds; rd += gridDim.z) {
