@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(32 * kMergeHeads, kCols == 16 ? 3 : 2) merge_k
                                                                  const float* __restrict__ part_l,
                                                                  Tout* __restrict__ o_lat,
                                                                  float* __restrict__ lse, int n_h, int d_c) {
-    pdl_trigger();                              // the kernel behind this one may set up
+    // The kernel behind this one may set up at once: it can then overlap only this kernel
+    // and the split kernel of the same call (which triggered after its own wait, so all
+    // before it is complete).
+    pdl_trigger();
     pdl_wait();                                 // launched behind the split kernel
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31;

@@ -137,10 +137,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    // the kernel behind this one in the same call may be scheduled now (it waits for this
-    // one's completion before it reads what this one writes)
-    pdl_trigger();
+    // The kernel behind this one may be scheduled once this one has waited for the kernel
+    // before it (a kernel launched beside this one reads its inputs before it waits, so
+    // everything before this kernel must be complete when it starts); beside the kernel
+    // before it (defer_wait), this one lets it in at once.
     if (!a.defer_wait) pdl_wait();
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // producer
@@ -281,7 +283,10 @@ append_finalize_kernel(const float* __restrict__ part, int k_splits, int n_tok, 
                        const int32_t* __restrict__ cap, const int32_t* __restrict__ pos0,
                        CacheView cv, int32_t* dev_status) {
     __shared__ float2 red[kFinGroups][kFinPairs];
-    pdl_trigger();              // a kernel behind this one may set up (it waits for this one to end)
+    // The kernel behind this one (the decode's query fold, beside the append) may start at
+    // once: the append GEMM let this kernel in only after its own wait, so all work before
+    // the append call is complete.
+    pdl_trigger();
     pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
     const int t = blockIdx.x;
     const int width = d_c + d_r;
@@ -360,7 +365,10 @@ append_finalize_fp8_kernel(const float* __restrict__ part, int k_splits, int n_t
                            uint8_t* __restrict__ cache, int64_t cache_rows, int32_t* dev_status) {
     __shared__ float2 red[kF8Groups][kF8Pairs];
     __shared__ float wmax[2];
-    pdl_trigger();              // a kernel behind this one may set up (it waits for this one to end)
+    // The kernel behind this one (the decode's query fold, beside the append) may start at
+    // once: the append GEMM let this kernel in only after its own wait, so all work before
+    // the append call is complete.
+    pdl_trigger();
     pdl_wait();                 // launched behind the append GEMM: its partial sums are complete
     const int t = blockIdx.x;
     const int width = d_c + d_r;

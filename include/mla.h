@@ -351,12 +351,14 @@ MLA_API mla_status mla_decode_prepare(const mla_dims* dims, mla_dtype dtype, int
                               void* o_lat, float* lse, int32_t* dev_status, void* stream);
 /*
  * mla_decode_prepare_beside -- mla_decode_prepare whose kernels may start while the
- * kernel enqueued before it on `stream` is still running (for instance the cache append
- * of the same step), so that the two run side by side on one stream.  The caller
- * guarantees that the work before it on the stream writes none of what this call reads
- * (q_c, q_r, w_uk, row_off, seq_len) and does not use `workspace`; every kernel of this
- * call ends only after that earlier kernel has ended, so work enqueued behind it (such as
- * mla_decode_attend) still sees everything before it complete.  Same arguments, errors
+ * kernels of the library call enqueued just before it on `stream` are still running (for
+ * instance the cache append of the same step), so that the two run side by side on one
+ * stream.  The caller guarantees that that call writes none of what this call reads
+ * (q_c, q_r, w_uk, row_off, seq_len) and does not use `workspace`.  Work enqueued before
+ * that call is complete when a kernel of this call starts (the library's kernels that wait
+ * for the kernel before them let the next one start only after that wait), and every
+ * kernel of this call ends only after that call's kernels have ended, so work enqueued
+ * behind it (such as mla_decode_attend) still sees everything before it complete.  Same arguments, errors
  * and effect as mla_decode_prepare.  Launch scheduling of the library, no step of the
  * method.
  */
