@@ -755,12 +755,18 @@ def run_reference(args, wl):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def named_workloads():
+    """Every workload --workload accepts: the named ones and each point of the sweep."""
+    import mla_inputs
+    return dict(mla_inputs.WORKLOADS, **{w.name: w for w in mla_inputs.sweep_workloads()})
+
+
 def main():
     args = parse()
     import mla_inputs
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    named = dict(mla_inputs.WORKLOADS, **{w.name: w for w in mla_inputs.sweep_workloads()})
+    named = named_workloads()
     if args.workload not in named:
         raise SystemExit(f"unknown workload {args.workload!r}; known: {', '.join(named)}")
     wl = named[args.workload]

@@ -39,7 +39,7 @@ constexpr int kWarps = 8, kTileRows = 32, kMaxColsPerLane = 16;
 
 struct SplitArgs {
     const float* qp; const void* cache; const int64_t* row_off; const int64_t* cum;
-    const Schedule* sched; const WorkerStart* wstart; void* o_lat; float* lse; float* part_o; float* part_l;
+    const WorkerStart* wstart; void* o_lat; float* lse; float* part_o; float* part_l;
     int n_h, d_c, d_r, batch;
 };
 
@@ -335,8 +335,8 @@ cudaError_t launch_split_simt(const mla_dims& d, bool bf16, int batch, int worke
                               const void* cache, const int64_t* row_off, const int64_t* cum,
                               const void* sched, const WorkerStart* wstart, void* o_lat, float* lse,
                               float* part_o, float* part_l, cudaStream_t s, bool fp8) {
-    SplitArgs a{qp, cache, row_off, cum, (const Schedule*)sched, wstart, o_lat, lse, part_o, part_l,
-                d.n_heads, d.d_c, d.d_r, batch};
+    (void)sched;                                // the kernel reads the start records instead
+    SplitArgs a{qp, cache, row_off, cum, wstart, o_lat, lse, part_o, part_l, d.n_heads, d.d_c, d.d_r, batch};
     const int dq = d.d_c + d.d_r;
     const size_t smem = (size_t)(kTileRows * (dq + 1) + kWarps * dq) * sizeof(float);
     dim3 grid(workers, (d.n_heads + kWarps - 1) / kWarps);

@@ -53,3 +53,13 @@ def test_clock_summary_keeps_only_samples_inside_the_windows():
     assert s["samples"] == 2 and s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
     s = cs.summary([(5.0, 6.0)])
     assert s["samples"] == 0 and s["sm_mhz"] is None and s["error"]
+
+
+def test_named_workloads_cover_configs_and_sweep_points():
+    named = bench.named_workloads()
+    for name in ("tiny_f32", "small_bf16", "v3_b64_l4096", "v3_ragged_b16", "v3_sweep_b128_l8192"):
+        assert name in named
+    sweep = [n for n in named if n.startswith("v3_sweep_")]
+    assert len(sweep) == len(mla_inputs.SWEEP_BATCHES) * len(mla_inputs.SWEEP_CONTEXTS)
+    w = named["v3_sweep_b256_l32768"]
+    assert (w.batch, w.prefill, w.seed) == (256, 32768, 4)
