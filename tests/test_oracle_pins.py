@@ -482,3 +482,24 @@ def test_pin_fp8_row_quantization():
     deq = mo.dequantize_row_fp8(vals, scales, k_r)
     assert deq.shape == row.shape
     assert np.max(np.abs(deq[:, :d_c] - row[:, :d_c])) <= 0.0625 * np.max(np.abs(row[:, :d_c]))
+
+
+def test_pin_fp8_scale_boundaries():
+    """Closed forms of the group scale (the smallest power of two 2^k with amax / 2^k <= 448):
+    amax 448 -> 1, 448 (1 + 2^-20) -> 2, 896 -> 2, 224 -> 1/2, 2^-20 -> 2^-28; a sign flip
+    changes nothing but the signs; the largest magnitude itself lands on a grid value."""
+    d_c, d_r = 256, 8
+    cases = [(448.0, 1.0), (448.0 * (1 + 2.0 ** -20), 2.0), (896.0, 2.0), (224.0, 0.5), (2.0 ** -20, 2.0 ** -28)]
+    for amax, want in cases:
+        row = np.zeros((1, d_c + d_r))
+        row[0, 5] = amax
+        row[0, 130] = -amax                      # second group, negative maximum
+        row[0, 7] = amax / 3.0
+        vals, scales, _ = mo.quantize_row_fp8(row, d_c)
+        assert scales.tolist() == [[want, want]], (amax, scales)
+        assert vals[0, 5] == -vals[0, 130]
+        assert mo.E4M3_MAX / 2 <= abs(vals[0, 5]) <= mo.E4M3_MAX
+        back = mo.dequantize_row_fp8(vals, scales, np.zeros((1, d_r)))
+        # one grid step of E4M3 near amax / scale is 2^(e - 3) with amax / scale in [2^e, 2^(e+1))
+        step = 2.0 ** (np.floor(np.log2(amax / want)) - 3) * want
+        assert abs(back[0, 7] - amax / 3.0) <= step / 2 * (1 + 1e-9)
