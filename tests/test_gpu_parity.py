@@ -370,3 +370,17 @@ def test_host_errors():
                               st.row_off, st.seq_len, st.max_seq_len, 0, st.workspace, st.ws_bytes,
                               st.o_lat, st.lse, st.dev_status)
     assert e.value.status == L.MLA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("num_splits", [5, 6, 12])
+def test_worker_ranges_starting_on_sequence_boundaries(num_splits):
+    """Lengths 100, 100, 100, 300 cut into equal ranges: with 6 (or 12) workers every range
+    boundary falls exactly on a sequence start or inside the long sequence, with 5 none
+    does; each worker's start record (first sequence, its span and first row) must still
+    lead to the right rows."""
+    base = mla_inputs.WORKLOADS["small_bf16"]
+    lens = [99, 99, 99, 299]
+    wl = dataclasses.replace(base, name="small_bf16_boundaries", batch=len(lens), n_new=1)
+    st = _run(wl, ctx_lens=lens, num_splits=num_splits)
+    for b in range(len(lens)):
+        _compare(st, wl, b, what=f" splits={num_splits}")
