@@ -775,9 +775,14 @@ split_tc_kernel(const __grid_constant__ CUtensorMap map_c128, const __grid_const
                 // code * scale is exact in bf16: the scale is a power of two (an integer-only
                 // form that adds the exponent to the code's bits measured slower than these
                 // conversions)
-    #pragma unroll
+    #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
-                    const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};   // 16 codes, lowest column first
+                    // one code vector a round, the next ones moved down (a rolled loop keeps
+                    // the conversion's code small)
+                    const uint4 vc = v[0];
+    #pragma unroll
+                    for (int q = 0; q < 7; ++q) v[q] = v[q + 1];
+                    const uint32_t w[4] = {vc.x, vc.y, vc.z, vc.w};   // 16 codes, lowest column first
                     uint32_t o[8];
     #pragma unroll
                     for (int e = 0; e < 8; ++e) {
